@@ -1,0 +1,215 @@
+"""Thin ctypes binding of libattn_paged.so (include/attn_paged.h).
+
+Argument marshalling only: every step of the attention runs in the library's CUDA
+kernels.  Functions keep the C names.  Tensors are torch tensors (device memory and
+streams come from PyTorch); the binding passes their raw pointers.  If the library
+cannot be loaded the import fails loudly: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_WORKSPACE = -3
+ATTN_ERR_CUDA = -4
+ATTN_KV_BF16 = 0
+ATTN_KV_FP8_E4M3 = 1
+
+EXPORTED = ("attn_plan", "attn_run_paged", "attn_run_phase", "attn_plan_destroy", "attn_get_device_error",
+            "attn_status_string", "attn_plan_host", "attn_plan_info", "attn_plan_blocks",
+            "attn_plan_segments")
+
+
+class attn_problem_t(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim_qk", ctypes.c_int32),
+                ("head_dim_v", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("page_table_stride", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int), ("window", ctypes.c_int32),
+                ("has_sinks", ctypes.c_int32),
+                ("qo_indptr_host", ctypes.POINTER(ctypes.c_int32)),
+                ("seq_lens_host", ctypes.POINTER(ctypes.c_int32))]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {attn_status_string(status)} ({status})")
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libattn_paged.so (building it first when missing or stale)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.build() if build_if_missing else library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libattn_paged.so not found at {path}")
+    L = ctypes.CDLL(path)
+    vp, i32p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)
+    L.attn_plan.argtypes = [ctypes.POINTER(attn_problem_t), ctypes.c_int, ctypes.POINTER(vp),
+                            ctypes.POINTER(ctypes.c_size_t)]
+    L.attn_run_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, ctypes.c_float,
+                                 ctypes.c_float, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp]
+    L.attn_run_phase.argtypes = [vp, ctypes.c_int32] + L.attn_run_paged.argtypes[1:]
+    L.attn_plan_destroy.argtypes = [vp]
+    L.attn_get_device_error.argtypes = [vp, vp, i32p]
+    L.attn_status_string.argtypes = [ctypes.c_int]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_plan_host.argtypes = [ctypes.POINTER(attn_problem_t), ctypes.c_int32, ctypes.POINTER(vp)]
+    L.attn_plan_info.argtypes = [vp, i32p]
+    L.attn_plan_blocks.argtypes = [vp, i32p]
+    L.attn_plan_segments.argtypes = [vp, i32p]
+    for name in EXPORTED:
+        if name != "attn_status_string":
+            getattr(L, name).restype = ctypes.c_int
+    _LIB = L
+    return L
+
+
+def attn_status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+class Plan:
+    """Owns an attn_plan_t handle (destroyed with the object)."""
+
+    def __init__(self, handle: int, workspace_bytes: int, device: int, keep):
+        self.handle = handle
+        self.workspace_bytes = workspace_bytes
+        self.device = device
+        self._keep = keep
+
+    def destroy(self) -> None:
+        if self.handle:
+            load().attn_plan_destroy(ctypes.c_void_p(self.handle))
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:  # interpreter shutdown
+            pass
+
+
+def make_problem(batch, num_q_heads, num_kv_heads, page_size, num_pages, page_table_stride,
+                 kv_dtype, window, has_sinks, qo_indptr, seq_lens, head_dim_qk=192,
+                 head_dim_v=128):
+    """Build an attn_problem_t from host int32 sequences (numpy arrays or lists)."""
+    import numpy as np
+    qo = np.ascontiguousarray(qo_indptr, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    p = attn_problem_t(batch, num_q_heads, num_kv_heads, head_dim_qk, head_dim_v, page_size,
+                       num_pages, page_table_stride, int(kv_dtype), window, int(bool(has_sinks)),
+                       qo.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                       sl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+    return p, (qo, sl)
+
+
+def attn_plan(problem: attn_problem_t, device: int, keep=None) -> Plan:
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(load().attn_plan(ctypes.byref(problem), int(device), ctypes.byref(h), ctypes.byref(ws)),
+           "attn_plan")
+    return Plan(h.value, ws.value, device, keep)
+
+
+def attn_plan_host(problem: attn_problem_t, num_sms: int, keep=None) -> Plan:
+    h = ctypes.c_void_p()
+    _check(load().attn_plan_host(ctypes.byref(problem), int(num_sms), ctypes.byref(h)),
+           "attn_plan_host")
+    return Plan(h.value, 0, -1, keep)
+
+
+def attn_plan_destroy(plan: Plan) -> None:
+    plan.destroy()
+
+
+def _run_args(plan, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks, window,
+              softmax_scale, k_scale, v_scale, out, lse_out, workspace, stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seq_lens),
+            _ptr(qo_indptr), _ptr(sinks), int(window), float(softmax_scale), float(k_scale),
+            float(v_scale), _ptr(out), _ptr(lse_out), _ptr(workspace), ws_bytes,
+            ctypes.c_void_p(int(stream)))
+
+
+def attn_run_paged(plan: Plan, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks,
+                   window: int, softmax_scale: float, k_scale: float, v_scale: float, out,
+                   lse_out=None, workspace=None, stream=None) -> None:
+    """Launch on `stream` (a torch.cuda.Stream, a raw handle, or None for torch's
+    current stream).  Pointer-only; nothing is synchronised."""
+    args = _run_args(plan, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks, window,
+                     softmax_scale, k_scale, v_scale, out, lse_out, workspace, stream)
+    _check(load().attn_run_paged(ctypes.c_void_p(plan.handle), *args), "attn_run_paged")
+
+
+def attn_run_phase(plan: Plan, phase: int, q, k_cache, v_cache, page_table, seq_lens,
+                   qo_indptr, sinks, window: int, softmax_scale: float, k_scale: float,
+                   v_scale: float, out, lse_out=None, workspace=None, stream=None) -> None:
+    """One of the two launches of attn_run_paged (0: split-KV kernel, 1: merge)."""
+    args = _run_args(plan, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks, window,
+                     softmax_scale, k_scale, v_scale, out, lse_out, workspace, stream)
+    _check(load().attn_run_phase(ctypes.c_void_p(plan.handle), int(phase), *args),
+           "attn_run_phase")
+
+
+def attn_get_device_error(plan: Plan) -> int:
+    err = ctypes.c_int32()
+    _check(load().attn_get_device_error(ctypes.c_void_p(plan.handle), None, ctypes.byref(err)),
+           "attn_get_device_error")
+    return err.value
+
+
+def attn_plan_info(plan: Plan) -> dict:
+    info = (ctypes.c_int32 * 8)()
+    _check(load().attn_plan_info(ctypes.c_void_p(plan.handle), info), "attn_plan_info")
+    return dict(blocks=info[0], segments=info[1], ctas=info[2], rows_per_block=info[3],
+                key_tile=info[4], multi_split_blocks=info[5],
+                workspace_bytes=(info[7] << 31) | info[6])
+
+
+def attn_plan_blocks(plan: Plan):
+    import numpy as np
+    n = attn_plan_info(plan)["blocks"]
+    arr = np.zeros((max(n, 1), 8), np.int32)
+    _check(load().attn_plan_blocks(ctypes.c_void_p(plan.handle),
+                                   arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+           "attn_plan_blocks")
+    return arr[:n]
+
+
+def attn_plan_segments(plan: Plan):
+    import numpy as np
+    n = attn_plan_info(plan)["segments"]
+    arr = np.zeros((max(n, 1), 5), np.int32)
+    _check(load().attn_plan_segments(ctypes.c_void_p(plan.handle),
+                                     arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+           "attn_plan_segments")
+    return arr[:n]

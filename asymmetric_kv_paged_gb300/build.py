@@ -1,0 +1,80 @@
+"""Build the CUDA library libattn_paged.so in-tree (nvcc, sm_103a only).
+
+Objects and the shared library go to ``asymmetric_kv_paged_gb300/_build/<machine>/``;
+translation units compile in parallel.  The CUDA runtime is linked statically and
+the driver API is reached through the runtime's entry-point query, so the library
+loads (and its symbols can be listed) on a machine without a GPU.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import platform
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+SOURCES = ["api.cu", "split_kv.cu", "merge.cu", "planner.cpp"]
+HEADERS = ["plan.hpp", "kernels.hpp"]
+
+
+def build_dir() -> str:
+    return os.path.join(PKG, "_build", platform.machine())
+
+
+def lib_path() -> str:
+    return os.path.join(build_dir(), "libattn_paged.so")
+
+
+def _nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found")
+
+
+def _inputs_mtime() -> float:
+    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
+    files += [os.path.join(INCLUDE, "attn_paged.h"), os.path.abspath(__file__)]
+    return max(os.path.getmtime(f) for f in files)
+
+
+def _compile(src: str, obj: str) -> None:
+    path = os.path.join(CSRC, src)
+    if src.endswith(".cpp"):
+        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", f"-I{INCLUDE}", f"-I{CSRC}",
+               "-c", path, "-o", obj]
+    else:
+        cmd = [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+               "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}", "-c", path, "-o", obj]
+        if os.environ.get("AKP_PTXAS_VERBOSE"):
+            cmd.insert(1, "-Xptxas=-v")
+    subprocess.run(cmd, check=True)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    out = lib_path()
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= _inputs_mtime():
+        return out
+    bdir = build_dir()
+    os.makedirs(bdir, exist_ok=True)
+    objs = [os.path.join(bdir, os.path.splitext(s)[0] + ".o") for s in SOURCES]
+    with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 1)) as ex:
+        futs = [ex.submit(_compile, s, o) for s, o in zip(SOURCES, objs)]
+        for f in futs:
+            f.result()
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run([_nvcc(), *ARCH, "-shared", "-o", tmp, *objs], check=True)
+    os.replace(tmp, out)
+    if verbose:
+        print(f"built {out}", file=sys.stderr)
+    return out
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose=True)

@@ -1,0 +1,267 @@
+// C ABI of the paged-attention library (declared in include/attn_paged.h).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "attn_paged.h"
+#include "kernels.hpp"
+#include "plan.hpp"
+
+namespace {
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess) ok = true;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+void free_device(attn_plan_s *p) {
+  if (p->dev.blocks) cudaFree(p->dev.blocks);
+  p->dev = akp::DevicePlan{};
+}
+
+attn_status_t upload(attn_plan_s *p) {
+  const akp::HostPlan &hp = p->host;
+  const size_t b_bytes = align256(hp.blocks.size() * sizeof(akp::BlockDesc));
+  const size_t s_bytes = align256(hp.segs.size() * sizeof(akp::SegDesc));
+  const size_t c_bytes = align256(hp.cta_seg_begin.size() * sizeof(int32_t));
+  const size_t m_bytes = align256(hp.merge_items.size() * sizeof(akp::MergeItem));
+  const size_t e_bytes = 256;
+  const size_t total = b_bytes + s_bytes + c_bytes + m_bytes + e_bytes;
+  uint8_t *base = nullptr;
+  if (cudaMalloc(&base, total) != cudaSuccess) return ATTN_ERR_CUDA;
+  p->dev.blocks = reinterpret_cast<akp::BlockDesc *>(base);
+  p->dev.segs = reinterpret_cast<akp::SegDesc *>(base + b_bytes);
+  p->dev.cta_seg_begin = reinterpret_cast<int32_t *>(base + b_bytes + s_bytes);
+  p->dev.merge_items = reinterpret_cast<akp::MergeItem *>(base + b_bytes + s_bytes + c_bytes);
+  p->dev.err = reinterpret_cast<int32_t *>(base + b_bytes + s_bytes + c_bytes + m_bytes);
+  cudaError_t e = cudaSuccess;
+  if (!hp.blocks.empty())
+    e = cudaMemcpy(p->dev.blocks, hp.blocks.data(), hp.blocks.size() * sizeof(akp::BlockDesc),
+                   cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && !hp.segs.empty())
+    e = cudaMemcpy(p->dev.segs, hp.segs.data(), hp.segs.size() * sizeof(akp::SegDesc),
+                   cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(p->dev.cta_seg_begin, hp.cta_seg_begin.data(),
+                   hp.cta_seg_begin.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && !hp.merge_items.empty())
+    e = cudaMemcpy(p->dev.merge_items, hp.merge_items.data(),
+                   hp.merge_items.size() * sizeof(akp::MergeItem), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(p->dev.err, 0, e_bytes);
+  if (e == cudaSuccess) e = akp::prepare_kernels(hp);
+  if (e != cudaSuccess) {
+    free_device(p);
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_plan_host(const attn_problem_t *problem, int32_t num_sms, attn_plan_t *plan) {
+  if (!plan) return ATTN_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (!problem) return ATTN_ERR_INVALID_ARG;
+  attn_plan_s *p = new (std::nothrow) attn_plan_s();
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = akp::build_host_plan(problem, num_sms, &p->host);
+  if (st != ATTN_OK) {
+    delete p;
+    return st;
+  }
+  *plan = p;
+  return ATTN_OK;
+}
+
+attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *plan,
+                        size_t *workspace_bytes) {
+  if (!plan) return ATTN_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (!problem || !workspace_bytes || device < 0) return ATTN_ERR_INVALID_ARG;
+  DeviceGuard guard(device);
+  if (!guard.ok) return ATTN_ERR_CUDA;
+  int num_sms = 0;
+  if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  attn_plan_t p = nullptr;
+  attn_status_t st = attn_plan_host(problem, num_sms, &p);
+  if (st != ATTN_OK) return st;
+  p->device = device;
+  st = upload(p);
+  if (st != ATTN_OK) {
+    delete p;
+    return st;
+  }
+  *workspace_bytes = p->host.workspace_bytes;
+  *plan = p;
+  return ATTN_OK;
+}
+
+attn_status_t attn_plan_destroy(attn_plan_t plan) {
+  if (!plan) return ATTN_OK;
+  if (plan->device >= 0) {
+    DeviceGuard guard(plan->device);
+    cudaDeviceSynchronize();
+    free_device(plan);
+  }
+  delete plan;
+  return ATTN_OK;
+}
+
+static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const void *k_cache,
+                              const void *v_cache, const int32_t *page_table,
+                              const int32_t *seq_lens, const int32_t *qo_indptr,
+                              const float *sinks, int32_t window, float softmax_scale,
+                              float k_scale, float v_scale, void *out, float *lse_out,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+  if (!plan || plan->device < 0) return ATTN_ERR_INVALID_ARG;
+  const akp::HostPlan &hp = plan->host;
+  const attn_problem_t &pr = hp.prob;
+  const bool has_rows = hp.qo_indptr.back() > 0;
+  if (has_rows && (!q || !k_cache || !v_cache || !page_table || !seq_lens || !qo_indptr || !out))
+    return ATTN_ERR_INVALID_ARG;
+  if (window != pr.window) return ATTN_ERR_INVALID_ARG;
+  if ((sinks != nullptr) != (pr.has_sinks != 0)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < hp.workspace_bytes || (hp.workspace_bytes && !workspace))
+    return ATTN_ERR_WORKSPACE;
+  if (!has_rows) return ATTN_OK;
+
+  const bool fp8 = pr.kv_dtype == ATTN_KV_FP8_E4M3;
+  akp::RunArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.page_table = page_table;
+  a.sinks = sinks;
+  a.scale_log2 = softmax_scale * (fp8 ? k_scale : 1.f) * 1.4426950408889634f;
+  a.v_scale = fp8 ? v_scale : 1.f;
+  a.out = out;
+  a.lse_out = lse_out;
+  a.part_o = static_cast<float *>(workspace);
+  a.part_lse = hp.part_rows ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                                        akp::part_o_bytes(hp.part_rows))
+                            : nullptr;
+  a.blocks = plan->dev.blocks;
+  a.segs = plan->dev.segs;
+  a.cta_seg_begin = plan->dev.cta_seg_begin;
+  a.merge_items = plan->dev.merge_items;
+  a.hq = pr.num_q_heads;
+  a.hkv = pr.num_kv_heads;
+  a.group = hp.group;
+  a.page_size = pr.page_size;
+  a.pt_stride = pr.page_table_stride;
+  a.num_pages = pr.num_pages;
+  a.window = pr.window;
+  a.err = plan->dev.err;
+
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return ATTN_ERR_CUDA;
+  DeviceGuard guard(cur == plan->device ? cur : plan->device);
+  if (!guard.ok) return ATTN_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((phases & 1) && akp::launch_split_kv(hp, a, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  if ((phases & 2) && akp::launch_merge(hp, a, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status_t attn_run_paged(attn_plan_t plan, const void *q, const void *k_cache,
+                             const void *v_cache, const int32_t *page_table,
+                             const int32_t *seq_lens, const int32_t *qo_indptr,
+                             const float *sinks, int32_t window, float softmax_scale,
+                             float k_scale, float v_scale, void *out, float *lse_out,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+  return run_impl(plan, 3, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks, window,
+                  softmax_scale, k_scale, v_scale, out, lse_out, workspace, workspace_bytes,
+                  stream);
+}
+
+attn_status_t attn_run_phase(attn_plan_t plan, int32_t phase, const void *q,
+                             const void *k_cache, const void *v_cache,
+                             const int32_t *page_table, const int32_t *seq_lens,
+                             const int32_t *qo_indptr, const float *sinks, int32_t window,
+                             float softmax_scale, float k_scale, float v_scale, void *out,
+                             float *lse_out, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+  if (phase != 0 && phase != 1) return ATTN_ERR_INVALID_ARG;
+  return run_impl(plan, phase == 0 ? 1 : 2, q, k_cache, v_cache, page_table, seq_lens,
+                  qo_indptr, sinks, window, softmax_scale, k_scale, v_scale, out, lse_out,
+                  workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_get_device_error(attn_plan_t plan, void *workspace, int32_t *err) {
+  (void)workspace;
+  if (!plan || !err || plan->device < 0) return ATTN_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return ATTN_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, plan->dev.err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (cudaMemset(plan->dev.err, 0, sizeof v) != cudaSuccess) return ATTN_ERR_CUDA;
+  *err = v;
+  return ATTN_OK;
+}
+
+const char *attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported problem";
+    case ATTN_ERR_WORKSPACE: return "workspace too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+attn_status_t attn_plan_info(attn_plan_t plan, int32_t info[8]) {
+  if (!plan || !info) return ATTN_ERR_INVALID_ARG;
+  const akp::HostPlan &hp = plan->host;
+  info[0] = (int32_t)hp.blocks.size();
+  info[1] = (int32_t)hp.segs.size();
+  info[2] = hp.num_ctas;
+  info[3] = (int32_t)hp.shape;
+  info[4] = akp::kKeyTile;
+  info[5] = hp.multi_split_blocks;
+  info[6] = (int32_t)(hp.workspace_bytes & 0x7FFFFFFF);
+  info[7] = (int32_t)(hp.workspace_bytes >> 31);
+  return ATTN_OK;
+}
+
+attn_status_t attn_plan_blocks(attn_plan_t plan, int32_t *blocks_host) {
+  if (!plan || (!blocks_host && !plan->host.blocks.empty())) return ATTN_ERR_INVALID_ARG;
+  int32_t *d = blocks_host;
+  for (const akp::BlockDesc &b : plan->host.blocks) {
+    const int32_t v[8] = {b.b, b.g, b.row0, b.nrows, b.klo, b.khi, b.num_splits, b.part_row_base};
+    std::memcpy(d, v, sizeof v);
+    d += 8;
+  }
+  return ATTN_OK;
+}
+
+attn_status_t attn_plan_segments(attn_plan_t plan, int32_t *segments_host) {
+  if (!plan || (!segments_host && !plan->host.segs.empty())) return ATTN_ERR_INVALID_ARG;
+  int32_t *d = segments_host;
+  for (size_t i = 0; i < plan->host.segs.size(); ++i) {
+    const akp::SegDesc &s = plan->host.segs[i];
+    const int32_t v[5] = {plan->host.seg_cta[i], s.block, s.tile_begin, s.tile_end, s.split};
+    std::memcpy(d, v, sizeof v);
+    d += 5;
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"

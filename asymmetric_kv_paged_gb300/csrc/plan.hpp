@@ -1,0 +1,87 @@
+// Internal plan layout shared by the host planner, the C ABI and the kernels.
+// Not part of the public ABI (see include/attn_paged.h).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "attn_paged.h"
+
+namespace akp {
+
+constexpr int kDqk = 192;       // query/key head dim
+constexpr int kDv = 128;        // value head dim
+constexpr int kKeyTile = 64;    // keys per pipeline tile
+
+// Row-block shapes of the split-KV kernel.  A block packs `rows` query rows of
+// one (request, KV head): row r <-> (token r / G, head g*G + r % G).
+enum class Shape : int32_t {
+  kRows16 = 16,    // decode: 4 warps split each key tile, one 16-row group
+  kRows64 = 64,    // verify: 4 warps x 16 rows, every warp sees the whole tile
+  kRows128 = 128,  // prefill: 8 warps x 16 rows
+};
+
+// One row block: rows [row0, row0 + nrows) of (b, g).  Keys [klo, khi) are
+// the union of what its rows can see.
+struct BlockDesc {
+  int32_t b, g, row0, nrows;
+  int32_t L, n, tok0, klo;        // seq len, new tokens, first flat token, first key
+  int32_t khi, num_splits, part_row_base, pad0;
+};
+static_assert(sizeof(BlockDesc) == 48, "BlockDesc layout");
+
+// One work segment: key tiles [tile_begin, tile_end) of one block.
+// split = index of this segment among the block's segments.
+struct SegDesc {
+  int32_t block, tile_begin, tile_end, split;
+};
+
+// One merge item: rows [row_begin, row_begin + 8) of a multi-split block.
+struct MergeItem {
+  int32_t block, row_begin;
+};
+constexpr int kMergeRowsPerCta = 8;
+
+struct HostPlan {
+  attn_problem_t prob{};
+  std::vector<int32_t> qo_indptr, seq_lens;
+  int32_t group = 1;             // G = Hq / Hkv
+  Shape shape = Shape::kRows16;
+  int32_t num_sms = 0, num_ctas = 0, threads = 0;
+  std::vector<BlockDesc> blocks;
+  std::vector<SegDesc> segs;
+  std::vector<int32_t> seg_cta;        // CTA of each segment
+  std::vector<int32_t> cta_seg_begin;  // [num_ctas + 1]
+  std::vector<MergeItem> merge_items;
+  int64_t part_rows = 0;
+  size_t workspace_bytes = 0;
+  int32_t multi_split_blocks = 0;
+};
+
+// Device-side copy of a plan (owned by attn_plan_s).
+struct DevicePlan {
+  BlockDesc *blocks = nullptr;
+  SegDesc *segs = nullptr;
+  int32_t *cta_seg_begin = nullptr;
+  MergeItem *merge_items = nullptr;
+  int32_t *err = nullptr;  // device error word
+};
+
+// Validate `p` and build the schedule for a device with num_sms SMs.
+attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan *out);
+
+// Workspace carve-up: partial outputs then partial lse, each 256-B aligned.
+inline size_t part_o_bytes(int64_t part_rows) {
+  return ((size_t)part_rows * kDv * sizeof(float) + 255) & ~(size_t)255;
+}
+inline size_t part_lse_bytes(int64_t part_rows) {
+  return ((size_t)part_rows * sizeof(float) + 255) & ~(size_t)255;
+}
+
+}  // namespace akp
+
+struct attn_plan_s {
+  akp::HostPlan host;
+  akp::DevicePlan dev;
+  int device = -1;     // -1: host-only plan (attn_plan_host)
+};

@@ -1,0 +1,160 @@
+// Host planner: validates a problem and turns it into row blocks, key-tile
+// segments per CTA, and a workspace layout.
+//
+// The split-KV schedule is the point of the pages' verify fix: the Triton
+// kernel they describe dropped split-KV whenever a request carried several
+// query tokens and left most SMs idle (MiMo-V2.6-Flash-RL model card, "What
+// the kernels do").  Here every (request, KV head) key range is cut into
+// tiles, and the tiles of all blocks are dealt to CTAs in order so that each
+// CTA gets the same number of tiles, whatever the mode.  A block whose tiles
+// land on several CTAs becomes a multi-split block whose partials are merged
+// by log-sum-exp.  All query rows of a block (all draft tokens x all heads of
+// the group) ride on one pass over the keys ("one program per whole verify").
+#include <algorithm>
+#include <cstring>
+
+#include "plan.hpp"
+
+namespace akp {
+
+namespace {
+
+Shape choose_shape(const HostPlan &hp) {
+  int64_t max_rows = 0;
+  for (int32_t b = 0; b < hp.prob.batch; ++b) {
+    int64_t n = hp.qo_indptr[b + 1] - hp.qo_indptr[b];
+    max_rows = std::max<int64_t>(max_rows, n * hp.group);
+  }
+  if (max_rows <= 16) return Shape::kRows16;
+  if (max_rows <= 64) return Shape::kRows64;
+  return Shape::kRows128;
+}
+
+int32_t threads_for(Shape s) { return s == Shape::kRows128 ? 256 : 128; }
+
+}  // namespace
+
+attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan *out) {
+  if (!p || !out || num_sms <= 0) return ATTN_ERR_INVALID_ARG;
+  if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->page_size <= 0 ||
+      p->num_pages <= 0 || p->page_table_stride <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (p->batch > 0 && (!p->qo_indptr_host || !p->seq_lens_host)) return ATTN_ERR_INVALID_ARG;
+  if (p->head_dim_qk != kDqk || p->head_dim_v != kDv) return ATTN_ERR_UNSUPPORTED;
+  if (p->num_q_heads % p->num_kv_heads != 0) return ATTN_ERR_UNSUPPORTED;
+  if (p->kv_dtype != ATTN_KV_BF16 && p->kv_dtype != ATTN_KV_FP8_E4M3) return ATTN_ERR_UNSUPPORTED;
+
+  HostPlan hp;
+  hp.prob = *p;
+  hp.num_sms = num_sms;
+  hp.group = p->num_q_heads / p->num_kv_heads;
+  hp.qo_indptr.assign(p->qo_indptr_host ? p->qo_indptr_host : nullptr,
+                      p->qo_indptr_host ? p->qo_indptr_host + p->batch + 1 : nullptr);
+  if (p->batch == 0) hp.qo_indptr.assign(1, 0);
+  hp.seq_lens.assign(p->seq_lens_host ? p->seq_lens_host : nullptr,
+                     p->seq_lens_host ? p->seq_lens_host + p->batch : nullptr);
+  hp.prob.qo_indptr_host = nullptr;
+  hp.prob.seq_lens_host = nullptr;
+  if (hp.qo_indptr[0] != 0) return ATTN_ERR_INVALID_ARG;
+  for (int32_t b = 0; b < p->batch; ++b) {
+    int64_t n = (int64_t)hp.qo_indptr[b + 1] - hp.qo_indptr[b];
+    int64_t L = hp.seq_lens[b];
+    if (n < 0 || L < n) return ATTN_ERR_INVALID_ARG;
+    if ((L + p->page_size - 1) / p->page_size > p->page_table_stride) return ATTN_ERR_INVALID_ARG;
+  }
+  // Flat row and tile counts must stay inside int32 device arithmetic.
+  if ((int64_t)hp.qo_indptr[p->batch] * p->num_q_heads > INT32_MAX / kDqk)
+    return ATTN_ERR_UNSUPPORTED;
+
+  hp.shape = choose_shape(hp);
+  hp.threads = threads_for(hp.shape);
+  const int32_t rows_per_block = (int32_t)hp.shape;
+  const int32_t G = hp.group;
+
+  // Row blocks.
+  int64_t total_tiles = 0;
+  for (int32_t b = 0; b < p->batch; ++b) {
+    const int32_t n = hp.qo_indptr[b + 1] - hp.qo_indptr[b];
+    const int32_t L = hp.seq_lens[b];
+    if (n == 0) continue;
+    const int32_t R = n * G;
+    for (int32_t g = 0; g < p->num_kv_heads; ++g) {
+      for (int32_t row0 = 0; row0 < R; row0 += rows_per_block) {
+        BlockDesc bd{};
+        bd.b = b;
+        bd.g = g;
+        bd.row0 = row0;
+        bd.nrows = std::min(rows_per_block, R - row0);
+        bd.L = L;
+        bd.n = n;
+        bd.tok0 = hp.qo_indptr[b];
+        const int32_t t_first = row0 / G;
+        const int32_t t_last = (row0 + bd.nrows - 1) / G;
+        const int64_t i_first = (int64_t)L - n + t_first;
+        const int64_t i_last = (int64_t)L - n + t_last;
+        int64_t lo = 0;
+        if (p->window > 0) lo = std::max<int64_t>(0, i_first - p->window + 1);
+        bd.klo = (int32_t)lo;
+        bd.khi = (int32_t)(i_last + 1);
+        total_tiles += (bd.khi - 1) / kKeyTile - bd.klo / kKeyTile + 1;
+        hp.blocks.push_back(bd);
+      }
+    }
+  }
+
+  // Deal tiles to CTAs in block order: each CTA takes `target` tiles, cutting
+  // a block where its share ends.  A block remainder of <= `slack` tiles is
+  // kept whole on the current CTA to avoid splits that cost more than they
+  // balance.
+  const int64_t nb = (int64_t)hp.blocks.size();
+  if (nb > 0) {
+    const int64_t min_tiles = 2;
+    int64_t target = std::max<int64_t>(min_tiles, (total_tiles + num_sms - 1) / num_sms);
+    const int64_t slack = std::max<int64_t>(1, target / 8);
+    int32_t cta = 0;
+    int64_t room = target;
+    for (int64_t bi = 0; bi < nb; ++bi) {
+      BlockDesc &bd = hp.blocks[bi];
+      int32_t t0 = bd.klo / kKeyTile;
+      const int32_t tend = (bd.khi - 1) / kKeyTile + 1;
+      int32_t split = 0;
+      while (t0 < tend) {
+        if (room <= 0) {
+          ++cta;
+          room = target;
+        }
+        int64_t left = tend - t0;
+        int64_t take = left <= room + slack ? left : room;
+        SegDesc s{(int32_t)bi, t0, (int32_t)(t0 + take), split++};
+        hp.segs.push_back(s);
+        hp.seg_cta.push_back(cta);
+        room -= take;
+        t0 += (int32_t)take;
+      }
+      bd.num_splits = split;
+    }
+    hp.num_ctas = cta + 1;
+  }
+  hp.cta_seg_begin.assign(hp.num_ctas + 1, 0);
+  for (size_t s = 0; s < hp.segs.size(); ++s) hp.cta_seg_begin[hp.seg_cta[s] + 1]++;
+  for (int32_t c = 0; c < hp.num_ctas; ++c) hp.cta_seg_begin[c + 1] += hp.cta_seg_begin[c];
+
+  // Partials and merge items for multi-split blocks.
+  for (int64_t bi = 0; bi < nb; ++bi) {
+    BlockDesc &bd = hp.blocks[bi];
+    bd.part_row_base = -1;
+    if (bd.num_splits > 1) {
+      bd.part_row_base = (int32_t)hp.part_rows;
+      hp.part_rows += (int64_t)bd.num_splits * bd.nrows;
+      hp.multi_split_blocks++;
+      for (int32_t r = 0; r < bd.nrows; r += kMergeRowsPerCta)
+        hp.merge_items.push_back(MergeItem{(int32_t)bi, r});
+    }
+  }
+  if (hp.part_rows > INT32_MAX / kDv) return ATTN_ERR_UNSUPPORTED;
+  hp.workspace_bytes = hp.part_rows ? part_o_bytes(hp.part_rows) + part_lse_bytes(hp.part_rows) : 0;
+  *out = std::move(hp);
+  return ATTN_OK;
+}
+
+}  // namespace akp

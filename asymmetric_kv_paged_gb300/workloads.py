@@ -5,8 +5,11 @@ and sink logits.  It holds none of the attention arithmetic, so the GPU tests,
 the benchmark and the CPU oracle can all consume the very same host bytes.
 
 Recipe (numpy PCG64, ``default_rng(seed)``), draw order fixed:
-  seq_lens -> per-request query counts -> page permutation -> q -> k -> v -> sinks.
-  * bf16 values are round-to-nearest-even of float32 N(0, std^2) draws.
+  seq_lens -> per-request query counts -> page permutation -> q -> kv_seed -> sinks.
+  * K and V values are float32 N(0, std^2), drawn row-chunk by row-chunk from
+    child generators of SeedSequence((kv_seed, 0)) and ((kv_seed, 1)), kv_seed
+    being the next draw of the main generator after q.
+  * bf16 values are round-to-nearest-even of the float32 draws.
   * fp8 K/V: float32 N(0,1) draws, per-tensor scale = amax / 448, codes are
     RNE(x / scale) in OCP E4M3 (torch's float8_e4m3fn cast; no overflow because
     |x / scale| <= 448).
@@ -35,10 +38,34 @@ POOL_SLOTS = 1_200_000
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
-    """float32 -> bf16 bit patterns, round to nearest even (finite inputs)."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    bias = ((u >> 16) & 1) + np.uint32(0x7FFF)
-    return ((u + bias) >> 16).astype(np.uint16)
+    """float32 -> bf16 bit patterns, round to nearest even (torch's CPU cast)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+_CHUNK = 32768
+
+
+def _draw_rows(seed: int, stream: int, rows: int, width: int, std: float) -> np.ndarray:
+    """float32 N(0, std^2) values [rows, width], drawn in chunks of 32768 rows from
+    child generators of SeedSequence((seed, stream)); chunks run on threads, the
+    values depend only on the seed."""
+    import concurrent.futures as cf
+    out = np.empty((rows, width), dtype=np.float32)
+    nchunks = (rows + _CHUNK - 1) // _CHUNK
+    children = np.random.SeedSequence((seed, stream)).spawn(max(nchunks, 1))
+
+    def fill(c: int) -> None:
+        lo, hi = c * _CHUNK, min(rows, (c + 1) * _CHUNK)
+        g = np.random.default_rng(children[c])
+        out[lo:hi] = g.standard_normal((hi - lo, width), dtype=np.float32)
+        if std != 1.0:
+            out[lo:hi] *= np.float32(std)
+
+    with cf.ThreadPoolExecutor(max_workers=min(16, max(1, nchunks))) as ex:
+        list(ex.map(fill, range(nchunks)))
+    return out
 
 
 def bf16_values(bits: np.ndarray) -> np.ndarray:
@@ -143,19 +170,18 @@ def make_workload(seed: int, seq_lens, n_per_req, hq: int, hkv: int, page_size: 
     slots = np.concatenate(slot_lists) if slot_lists else np.zeros(0, np.int64)
 
     nslot = num_pages * page_size
-    k_draw = rng.standard_normal((slots.size, hkv, DQK), dtype=np.float32)
-    v_draw = rng.standard_normal((slots.size, hkv, DV), dtype=np.float32)
+    kv_seed = int(rng.integers(0, 2**63 - 1))
+    k_vals = _draw_rows(kv_seed, 0, slots.size, hkv * DQK, k_std)
+    v_vals = _draw_rows(kv_seed, 1, slots.size, hkv * DV, v_std)
     if kv_dtype == "bf16":
-        k_cache = np.full((nslot, hkv, DQK), BF16_NAN, dtype=np.uint16)
-        v_cache = np.full((nslot, hkv, DV), BF16_NAN, dtype=np.uint16)
-        k_cache[slots] = bf16_bits(k_draw * np.float32(k_std))
-        v_cache[slots] = bf16_bits(v_draw * np.float32(v_std))
+        k_cache = np.full((nslot, hkv * DQK), BF16_NAN, dtype=np.uint16)
+        v_cache = np.full((nslot, hkv * DV), BF16_NAN, dtype=np.uint16)
+        k_cache[slots] = bf16_bits(k_vals)
+        v_cache[slots] = bf16_bits(v_vals)
         k_scale = v_scale = 1.0
     elif kv_dtype == "fp8":
-        k_cache = np.full((nslot, hkv, DQK), E4M3_NAN, dtype=np.uint8)
-        v_cache = np.full((nslot, hkv, DV), E4M3_NAN, dtype=np.uint8)
-        k_vals = k_draw * np.float32(k_std)
-        v_vals = v_draw * np.float32(v_std)
+        k_cache = np.full((nslot, hkv * DQK), E4M3_NAN, dtype=np.uint8)
+        v_cache = np.full((nslot, hkv * DV), E4M3_NAN, dtype=np.uint8)
         k_amax = float(np.abs(k_vals).max()) if k_vals.size else 1.0
         v_amax = float(np.abs(v_vals).max()) if v_vals.size else 1.0
         k_scale = float(np.float32(k_amax / 448.0)) or 1.0
@@ -164,7 +190,7 @@ def make_workload(seed: int, seq_lens, n_per_req, hq: int, hkv: int, page_size: 
         v_cache[slots] = e4m3_codes(v_vals / np.float32(v_scale))
     else:
         raise ValueError(kv_dtype)
-    del k_draw, v_draw
+    del k_vals, v_vals
 
     sink_arr = rng.standard_normal(hq, dtype=np.float32) if sinks else None
     if softmax_scale is None:

@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""Benchmark of paged asymmetric-KV attention (QK 192 / V 128) on one or more GPUs.
+
+Headline workload: batched paged decode (32 requests x 1 token, 16 q / 2 KV heads,
+context U[1024, 32768] not page aligned, page 128, bf16 K/V in a shuffled 1.2M-slot
+pool).  A step is one attn_run_paged call (split-KV kernel + log-sum-exp merge)
+over that batch; inputs are resident in HBM.  The KV stream (~0.7 GB) is far larger
+than L2 (129 MB), so no L2 flush is needed between steps.
+
+  value      algorithmic bytes per step x ranks / time per step (GB/s)
+  roofline   the split-KV kernel alone: algorithmic bytes / its own CUDA-event time
+  e2e        through the C ABI from pinned host buffers: q and the batch metadata
+             copied in, attn_run_paged, the output copied back, every step
+  extra      the other named workloads (tiny decode, verify at page 128 and 1,
+             SWA with sinks, fp8 chunked prefill) with their own roofline fraction
+  cpu_baseline  the FP64 oracle on a bounded sample of the headline workload
+
+Under torchrun every rank runs its own replica of the workload (independent
+requests: no collective on the data path) and the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode/verify KV-read GB/s & % HBM roofline; prefill TFLOP/s & % tensor peak"
+HEADLINE = "c2_batched_decode"
+DQK, DV = 192, 128
+
+
+# ---------------------------------------------------------------- accounting
+
+def algorithmic_bytes(w) -> int:
+    """Every visible key of every (request, KV head) once (K and V rows), Q in,
+    bf16 out, touched page-table entries and the sinks; split partials and
+    masked slots excluded."""
+    es = 2 if w.kv_dtype == "bf16" else 1
+    keys = 0
+    pages = 0
+    for b in range(w.batch):
+        lo, hi = w.visible_range(b)
+        if hi > lo:
+            keys += hi - lo
+            pages += (hi - 1) // w.page_size - lo // w.page_size + 1
+    total = keys * w.hkv * (DQK + DV) * es
+    total += w.total_q * w.hq * (DQK + DV) * 2
+    total += pages * 4
+    if w.sinks is not None:
+        total += w.hq * 4
+    return int(total)
+
+
+def algorithmic_flops(w) -> int:
+    """2 * (192 + 128) FLOPs per visible (query row, key) pair."""
+    pairs = 0
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        n = int(w.qo_indptr[b + 1] - w.qo_indptr[b])
+        i = L - n + np.arange(n, dtype=np.int64)
+        lo = np.maximum(0, i - w.window + 1) if w.window > 0 else np.zeros_like(i)
+        pairs += int((i + 1 - lo).sum())
+    return 2 * (DQK + DV) * pairs * w.hq
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def split_kernel_traffic(workload: str):
+    """DRAM bytes per launch of the split-KV kernel from a committed ncu summary,
+    when that summary was taken on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", f"split_kv_{workload}.md")
+    src = os.path.join(ROOT, "asymmetric_kv_paged_gb300", "csrc", "split_kv.cu")
+    if not os.path.exists(path):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_sha256_16") != digest:
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch_full_size"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5:
+            time.sleep(0.01)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        use = inside or [p for t, p in self.samples]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in use if num(p[0]) is not None]
+        mx = [num(p[1]) for p in use if num(p[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for p in use for n, v in zip(names, p[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- our arm
+
+def time_workload(dw, steps: int, warmup: int, world: int, flush_l2: bool = False,
+                  sampler=None):
+    """Returns dict with step ms, split/merge kernel ms (CUDA events on the launch
+    stream) and the wall-clock bounds of the timed region."""
+    import torch
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if flush_l2 else None
+    for _ in range(warmup):
+        dw.run_phase(0, stream)
+        dw.run_phase(1, stream)
+    has_merge = dw.plan.workspace_bytes > 0
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for k in range(steps):
+        if flush is not None:
+            flush.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        dw.run_phase(0, stream)
+        ev[k][1].record(stream)
+        dw.run_phase(1, stream)
+        ev[k][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    split = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    merge = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    attn = float(np.mean([e[0].elapsed_time(e[2]) for e in ev]))
+    total = start.elapsed_time(end) / steps
+    return dict(step_ms=(attn if flush_l2 else total), split_ms=split, merge_ms=merge,
+                attn_ms=attn, t0=t0, t1=t1, launches=steps * (2 if has_merge else 1))
+
+
+def e2e_measure(dw, steps: int, warmup: int, world: int):
+    """Per step: q, page table, seq_lens, qo_indptr copied host->device from pinned
+    buffers, attn_run_paged, out copied device->host.  The K/V cache is state and
+    stays resident."""
+    import torch
+    w = dw.w
+    stream = torch.cuda.current_stream()
+    h_q = torch.from_numpy(w.q).view(torch.bfloat16).pin_memory()
+    h_pt = torch.from_numpy(w.page_table).pin_memory()
+    h_sl = torch.from_numpy(w.seq_lens).pin_memory()
+    h_qo = torch.from_numpy(w.qo_indptr).pin_memory()
+    h_out = torch.empty(dw.out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_sl, h_qo))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def step():
+        dw.q.copy_(h_q, non_blocking=True)
+        dw.page_table.copy_(h_pt, non_blocking=True)
+        dw.seq_lens.copy_(h_sl, non_blocking=True)
+        dw.qo_indptr.copy_(h_qo, non_blocking=True)
+        dw.run(stream)
+        h_out.copy_(dw.out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    # plan cost (host planning + upload), once per batch shape; reported apart
+    t = time.time()
+    for _ in range(3):
+        dw.make_plan().destroy()
+    plan_ms = (time.time() - t) / 3 * 1e3
+    return dict(ms=start.elapsed_time(end) / steps, h2d=h2d, d2h=d2h, plan_ms=plan_ms)
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """The FP64 oracle, as it stands, on whole requests of the workload until about
+    budget_s of wall time has been spent."""
+    from oracle import oracle
+    pb = w.host_arrays()
+    done_bytes = 0
+    done_req = 0
+    t_total = 0.0
+    for b in range(w.batch):
+        toks = np.arange(w.qo_indptr[b], w.qo_indptr[b + 1], dtype=np.int64)
+        rows = (toks[:, None] * w.hq + np.arange(w.hq)[None, :]).reshape(-1)
+        t = time.time()
+        oracle.attn_paged(pb, rows=rows)
+        t_total += time.time() - t
+        lo, hi = w.visible_range(b)
+        done_bytes += (hi - lo) * w.hkv * (DQK + DV) * (2 if w.kv_dtype == "bf16" else 1)
+        done_bytes += len(toks) * w.hq * (DQK + DV) * 2
+        done_req += 1
+        if t_total >= budget_s:
+            break
+    return {"value": done_bytes / t_total / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{done_req} of {w.batch} requests of {w.name} (all their rows), "
+                      f"{t_total:.1f} s FP64 on host cores"}
+
+
+def measure_extra(name: str, pk: dict, steps: int, warmup: int, world: int):
+    import torch
+    from asymmetric_kv_paged_gb300 import workloads
+    from asymmetric_kv_paged_gb300.runner import DeviceWorkload
+    w = workloads.named(name)
+    dw = DeviceWorkload(w, device=torch.cuda.current_device())
+    nbytes = algorithmic_bytes(w)
+    flops = algorithmic_flops(w)
+    small = nbytes < 256e6          # fits in L2 across steps: flush between steps
+    r = time_workload(dw, steps, warmup, world, flush_l2=small)
+    if name.startswith("c5"):
+        achieved = flops / (r["split_ms"] * 1e-3) / 1e12
+        peak = pk["bf16_tflops"]
+        out = {"workload": name, "value": flops / (r["attn_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": r["attn_ms"], "roofline": {"bound": "tensor", "achieved": achieved,
+                                                           "peak": peak, "unit": "TFLOP/s",
+                                                           "frac": achieved / peak}}
+    else:
+        achieved = nbytes / (r["split_ms"] * 1e-3) / 1e9
+        peak = pk["hbm_gbs"]
+        out = {"workload": name, "value": nbytes / (r["attn_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": r["attn_ms"], "roofline": {"bound": "hbm", "achieved": achieved,
+                                                           "peak": peak, "unit": "GB/s",
+                                                           "frac": achieved / peak}}
+    out.update(split_ms=r["split_ms"], merge_ms=r["merge_ms"], algorithmic_bytes=nbytes,
+               flops=flops, l2="flushed between steps" if small else "inputs larger than L2")
+    del dw
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from asymmetric_kv_paged_gb300 import binding, workloads
+    from asymmetric_kv_paged_gb300.runner import DeviceWorkload
+    binding.load()
+    pk = peaks()
+    w = workloads.named(args.workload)
+    dw = DeviceWorkload(w, device=torch.cuda.current_device())
+    nbytes = algorithmic_bytes(w)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    r = time_workload(dw, args.steps, args.warmup, world)
+    clocks = sampler.summary(r["t0"], r["t1"]) if sampler else None
+    if sampler:
+        sampler.stop()
+    step_ms = max_over_ranks(r["step_ms"], world)
+    split_ms = max_over_ranks(r["split_ms"], world)
+    e2e = e2e_measure(dw, max(10, args.steps // 4), 3, world)
+    e2e_ms = max_over_ranks(e2e["ms"], world)
+    assert binding.attn_get_device_error(dw.plan) == 0
+
+    achieved = nbytes / (split_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": nbytes * world / (step_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64; bf16 N(0,1) values, K scaled 0.5)",
+        "config": {"workload": args.workload, "batch": w.batch, "q_tokens_per_request": 1,
+                   "num_q_heads": w.hq, "num_kv_heads": w.hkv, "head_dim_qk": DQK,
+                   "head_dim_v": DV, "page_size": w.page_size, "pool_slots": w.num_pages * w.page_size,
+                   "kv_tokens": int(w.seq_lens.sum()), "kv_dtype": w.kv_dtype,
+                   "algorithmic_bytes_per_step": nbytes,
+                   "l2": "inputs larger than L2 (KV stream per step >> 129 MB); no flush",
+                   "parallelism": f"replicas x{world} (independent requests, no collective)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": split_kernel_traffic(args.workload),
+                     "kernel": "split_kv_kernel", "kernel_ms": split_ms, "merge_ms": r["merge_ms"],
+                     "peak_source": f"{pk['source']} (hbm_gbs)"},
+        "e2e": {"value": nbytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": e2e_ms, "plan_ms_per_batch_shape": e2e["plan_ms"]},
+        "gpu_launches": r["launches"],
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_extra:
+        extra = []
+        for name in workloads.CONFIG_NAMES:
+            if name == args.workload:
+                continue
+            extra.append(measure_extra(name, pk, max(20, args.steps // 4), args.warmup, 1))
+        line["extra"] = extra
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The FP64 oracle as it stands, on the host cores: each step computes a bounded
+    sample (whole requests) of the headline workload."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    from asymmetric_kv_paged_gb300 import workloads
+    from oracle import oracle
+    w = workloads.named(args.workload)
+    pb = w.host_arrays()
+    reqs = list(range(min(2, w.batch)))          # ~1 s of FP64 work per step
+    rows = np.concatenate([
+        (np.arange(w.qo_indptr[b], w.qo_indptr[b + 1])[:, None] * w.hq
+         + np.arange(w.hq)[None, :]).reshape(-1) for b in reqs])
+    es = 2 if w.kv_dtype == "bf16" else 1
+    nbytes = sum((w.visible_range(b)[1] - w.visible_range(b)[0]) * w.hkv * (DQK + DV) * es
+                 + int(w.qo_indptr[b + 1] - w.qo_indptr[b]) * w.hq * (DQK + DV) * 2 for b in reqs)
+    for _ in range(args.warmup):
+        oracle.attn_paged(pb, rows=rows)
+    t = time.time()
+    for _ in range(args.steps):
+        oracle.attn_paged(pb, rows=rows)
+    dt = (time.time() - t) / args.steps
+    value = nbytes / dt / 1e9
+    sample = f"requests {reqs} of {w.name} ({len(rows)} rows) per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy PCG64)",
+            "config": {"workload": args.workload, "parallelism": "host cores (OpenMP)"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * attn_paged.h - C ABI of the GB300 (sm_103a) paged-attention library for
+ * models whose query/key head dim (192) differs from the value head dim (128).
+ *
+ * The operation (no page states a formula; this is the plainest reading of
+ * what the pages name, and the design notes list every reading):
+ *   For request b with n_b new tokens (qo_indptr[b+1] - qo_indptr[b]) and
+ *   L_b = seq_lens[b] keys in the cache (the n_b new tokens included, as the
+ *   last n_b keys), query token t in [0, n_b) and query head h:
+ *     g  = h / (Hq / Hkv)          (GQA: consecutive q heads share KV head g)
+ *     i  = L_b - n_b + t           (causal position of the token)
+ *     visible keys j: 0 <= j <= i and, when window > 0, j > i - window
+ *     k_j = K[page_table[b][j / P], j % P, g, :] * k_scale
+ *     v_j = V[page_table[b][j / P], j % P, g, :] * v_scale
+ *     s_j = softmax_scale * <q, k_j>
+ *     out = sum_j e^{s_j - m} v_j / (sum_j e^{s_j - m} + e^{sinks[h] - m}),
+ *     m = max(max_j s_j, sinks[h]); without sinks the sink term is absent.
+ *     lse = m + ln(denominator)  (natural log)
+ *
+ * Where the operation comes from:
+ *   - separate K and V caches of different row widths (192 vs 128): sglang
+ *     PR #32818, "Route asymmetric-KV models to fa4 on SM100" (the
+ *     trtllm_mha key_cache/value_cache size check, and has_asymmetric_kv);
+ *   - paged KV with page size 1 or 128, CUDA-graph replay: sglang PR #41886,
+ *     "Speed Tests and Profiling" and "Accuracy Tests";
+ *   - decode, 8-token verify, full vs sliding window with sinks, ragged page
+ *     boundaries: sglang PR #41886, "Accuracy Tests";
+ *   - split-KV kept on for multi-token verify, one program per whole verify,
+ *     FP8 E4M3 K/V converted in the load path, Q.K kept in 16-bit: the
+ *     MiMo-V2.6-Flash-RL 2x RTX PRO 6000 model card, "What the kernels do"
+ *     and "Things that were measured and did not help";
+ *   - unused KV tails may hold NaN and must be masked, not multiplied:
+ *     sammysun0711/sglang PR #35, "Modifications" (FlyPA V-tail masking).
+ *
+ * Conventions shared by every call:
+ *   - All pointers named *_host are host memory; all others are device memory
+ *     of the plan's device.  The caller owns every buffer it passes.
+ *   - Functions return a status and never abort the process.
+ *   - attn_run_paged never allocates, never synchronises and issues work only
+ *     on the given stream, so it can be captured in a CUDA graph.
+ */
+#ifndef ATTN_PAGED_H
+#define ATTN_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = -1,  /* a NULL pointer, inconsistent sizes, or a run
+                                   argument that does not match the plan */
+    ATTN_ERR_UNSUPPORTED = -2,  /* head dims other than 192/128, Hq % Hkv != 0 */
+    ATTN_ERR_WORKSPACE = -3,    /* workspace smaller than attn_plan reported */
+    ATTN_ERR_CUDA = -4          /* a CUDA runtime error (allocation in attn_plan,
+                                   or a launch error in attn_run_paged) */
+} attn_status_t;
+
+typedef enum {
+    ATTN_KV_BF16 = 0,      /* K/V elements are bfloat16 */
+    ATTN_KV_FP8_E4M3 = 1   /* K/V elements are OCP FP8 E4M3 codes; value =
+                              decoded code * k_scale (resp. v_scale) */
+} attn_kv_dtype_t;
+
+typedef struct attn_plan_s *attn_plan_t;
+
+/*
+ * Problem description, copied by attn_plan (the caller may free the host
+ * arrays afterwards).
+ *   batch               B >= 0 requests.
+ *   num_q_heads         Hq; num_kv_heads Hkv; Hq % Hkv == 0.
+ *   head_dim_qk         must be 192; head_dim_v must be 128.
+ *   page_size           P >= 1 tokens per page.
+ *   num_pages           pages in each of the K and V pools.
+ *   page_table_stride   int32 entries per request row of the page table; must
+ *                       be >= ceil(seq_lens[b] / P) for every b.
+ *   kv_dtype            element type of both caches.
+ *   window              <= 0: full causal attention; > 0: the query at
+ *                       position i sees keys j with i - window < j <= i
+ *                       (window keys, itself included).
+ *   has_sinks           nonzero: attn_run_paged takes a per-head sink logit.
+ *   qo_indptr_host      [B+1] int32, qo_indptr[0] = 0, non-decreasing.
+ *   seq_lens_host       [B] int32, seq_lens[b] >= qo_indptr[b+1]-qo_indptr[b].
+ */
+typedef struct {
+    int32_t batch, num_q_heads, num_kv_heads;
+    int32_t head_dim_qk, head_dim_v;
+    int32_t page_size, num_pages, page_table_stride;
+    attn_kv_dtype_t kv_dtype;
+    int32_t window;
+    int32_t has_sinks;
+    const int32_t *qo_indptr_host;
+    const int32_t *seq_lens_host;
+} attn_problem_t;
+
+/*
+ * Build a plan for one batch shape on CUDA device `device`.
+ * Splits every (request, KV head) key range into work segments sized for the
+ * device's SM count, uploads the work list to device memory owned by the plan,
+ * and reports the workspace size attn_run_paged needs (may be 0).
+ * Synchronous; allocates device memory.  Errors: INVALID_ARG (NULL pointers,
+ * inconsistent lengths), UNSUPPORTED (head dims), CUDA (device errors).
+ * On error *plan is set to NULL.
+ */
+attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *plan,
+                        size_t *workspace_bytes);
+
+/*
+ * Run the planned attention on `stream`.
+ *   q            bf16 [total_q, Hq, 192], row-major, contiguous.
+ *   k_cache      [num_pages, P, Hkv, 192] of bf16 or E4M3 bytes.
+ *   v_cache      [num_pages, P, Hkv, 128] of the same type.
+ *   page_table   int32 [B, page_table_stride]; entries at or beyond
+ *                ceil(seq_lens[b] / P) are never read.  Page ids outside
+ *                [0, num_pages) are not dereferenced: the rows they would
+ *                supply are read as zero and the plan's device error word
+ *                records the fault (attn_get_device_error).
+ *   seq_lens     int32 [B] device copy; qo_indptr int32 [B+1] device copy.
+ *                Both must equal the host arrays the plan was built from: the
+ *                kernels take lengths from the plan's own device copy.
+ *   sinks        fp32 [Hq] sink logits in the units of the scaled scores, or
+ *                NULL; must be non-NULL exactly when the plan has_sinks.
+ *   window       must equal the plan's window.
+ *   softmax_scale, k_scale, v_scale  as in the operation above (the kv scales
+ *                are ignored for bf16 caches and should be 1).
+ *   out          bf16 [total_q, Hq, 128].
+ *   lse_out      fp32 [total_q, Hq] natural-log denominators, or NULL.
+ *   workspace    device scratch of at least workspace_bytes (may be NULL when
+ *                the plan reported 0).  Its contents need no initialisation.
+ * Slots of the caches that no query can see are never read, so they may hold
+ * anything (NaN included).  Queries are read as bf16; with an FP8 cache the
+ * products are formed in fp16 (|q| must stay below 65504).
+ * Runs of one plan must be ordered on one stream (they share the plan's
+ * device error word); different plans are independent.
+ * Errors: INVALID_ARG, WORKSPACE, CUDA (launch errors; nothing is waited for).
+ */
+attn_status_t attn_run_paged(attn_plan_t plan, const void *q, const void *k_cache,
+                             const void *v_cache, const int32_t *page_table,
+                             const int32_t *seq_lens, const int32_t *qo_indptr,
+                             const float *sinks, int32_t window, float softmax_scale,
+                             float k_scale, float v_scale, void *out, float *lse_out,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The two launches attn_run_paged makes, one at a time, for callers that time
+ * or interleave them: phase 0 is the split-KV attention kernel, phase 1 the
+ * log-sum-exp merge of split partials (nothing is launched when the plan has
+ * no block split over several CTAs).  Arguments, validation and errors are
+ * those of attn_run_paged; phase 0 then phase 1 on one stream is exactly
+ * attn_run_paged.  Other phase values: INVALID_ARG.
+ */
+attn_status_t attn_run_phase(attn_plan_t plan, int32_t phase, const void *q,
+                             const void *k_cache, const void *v_cache,
+                             const int32_t *page_table, const int32_t *seq_lens,
+                             const int32_t *qo_indptr, const float *sinks, int32_t window,
+                             float softmax_scale, float k_scale, float v_scale, void *out,
+                             float *lse_out, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/* Free a plan and its device memory (synchronises the plan's device).
+ * NULL is accepted. */
+attn_status_t attn_plan_destroy(attn_plan_t plan);
+
+/*
+ * Read and clear the plan's device error word (synchronous).  Bit 0: a page
+ * id outside [0, num_pages) was met.  The workspace argument is unused and
+ * may be NULL.
+ */
+attn_status_t attn_get_device_error(attn_plan_t plan, void *workspace, int32_t *err);
+
+/* Static text for a status code. */
+const char *attn_status_string(attn_status_t status);
+
+/*
+ * Host-side inspection of the schedule, for tests and tools (no GPU needed).
+ *
+ * attn_plan_host builds a plan on the host only, for a device with `num_sms`
+ * SMs; it cannot be run.  attn_plan_info reports its shape:
+ *   info[0] = number of row blocks, info[1] = number of work segments,
+ *   info[2] = number of CTAs, info[3] = rows per block (16, 64 or 128),
+ *   info[4] = key tile (keys per tile), info[5] = multi-split blocks,
+ *   info[6] = workspace bytes (low 31 bits in info[6], high bits in info[7]).
+ * attn_plan_blocks copies the blocks as 8 int32 each:
+ *   {b, g, row0, nrows, key_lo, key_hi, num_splits, part_row_base}
+ * and attn_plan_segments copies the segments as 5 int32 each:
+ *   {cta, block, tile_begin, tile_end, split}
+ * where tiles are absolute (tile T holds keys [T*tile, (T+1)*tile)).
+ * The destination arrays must hold info[0]*8 (resp. info[1]*5) int32.
+ */
+attn_status_t attn_plan_host(const attn_problem_t *problem, int32_t num_sms, attn_plan_t *plan);
+attn_status_t attn_plan_info(attn_plan_t plan, int32_t info[8]);
+attn_status_t attn_plan_blocks(attn_plan_t plan, int32_t *blocks_host);
+attn_status_t attn_plan_segments(attn_plan_t plan, int32_t *segments_host);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_PAGED_H */

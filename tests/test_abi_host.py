@@ -1,0 +1,145 @@
+"""C-ABI library checks that need no GPU: it loads, exports what the header
+declares, validates problems, and its schedule covers every visible key once."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from asymmetric_kv_paged_gb300 import binding as B
+from asymmetric_kv_paged_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(attn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = B.load()
+    declared = header_functions()
+    assert "attn_plan" in declared and "attn_run_paged" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(B.EXPORTED)
+
+
+def test_status_strings():
+    assert B.attn_status_string(0) == "ok"
+    assert "workspace" in B.attn_status_string(B.ATTN_ERR_WORKSPACE)
+
+
+def _problem(**kw):
+    base = dict(batch=2, num_q_heads=16, num_kv_heads=2, page_size=16, num_pages=100,
+                page_table_stride=8, kv_dtype=B.ATTN_KV_BF16, window=0, has_sinks=False,
+                qo_indptr=[0, 1, 9], seq_lens=[100, 120])
+    base.update(kw)
+    return B.make_problem(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim_qk=128), B.ATTN_ERR_UNSUPPORTED),
+    (dict(head_dim_v=192), B.ATTN_ERR_UNSUPPORTED),
+    (dict(num_q_heads=15), B.ATTN_ERR_UNSUPPORTED),
+    (dict(seq_lens=[100, 5]), B.ATTN_ERR_INVALID_ARG),          # L < n
+    (dict(qo_indptr=[0, 3, 2]), B.ATTN_ERR_INVALID_ARG),        # non-monotone
+    (dict(qo_indptr=[1, 2, 9]), B.ATTN_ERR_INVALID_ARG),        # must start at 0
+    (dict(seq_lens=[100, 129]), B.ATTN_ERR_INVALID_ARG),        # needs 9 pages > stride 8
+    (dict(page_size=0), B.ATTN_ERR_INVALID_ARG),
+    (dict(num_kv_heads=0), B.ATTN_ERR_INVALID_ARG),
+])
+def test_plan_rejects_bad_problems(kw, status):
+    prob, keep = _problem(**kw)
+    with pytest.raises(B.AttnError) as e:
+        B.attn_plan_host(prob, 152, keep)
+    assert e.value.status == status
+
+
+def _coverage_check(w, num_sms):
+    prob, keep = B.make_problem(
+        batch=w.batch, num_q_heads=w.hq, num_kv_heads=w.hkv, page_size=w.page_size,
+        num_pages=w.num_pages, page_table_stride=w.page_table.shape[1],
+        kv_dtype=B.ATTN_KV_BF16, window=w.window, has_sinks=False, qo_indptr=w.qo_indptr,
+        seq_lens=w.seq_lens)
+    plan = B.attn_plan_host(prob, num_sms, keep)
+    info = B.attn_plan_info(plan)
+    blocks = B.attn_plan_blocks(plan)
+    segs = B.attn_plan_segments(plan)
+    tile = info["key_tile"]
+    R = info["rows_per_block"]
+    G = w.hq // w.hkv
+    assert info["ctas"] <= num_sms
+    # every (b, g, row) lives in exactly one block; block key range = union of its rows' keys
+    seen = set()
+    for (b, g, row0, nrows, klo, khi, nsplit, prb) in blocks:
+        n = int(w.qo_indptr[b + 1] - w.qo_indptr[b])
+        L = int(w.seq_lens[b])
+        assert 0 < nrows <= R
+        for r in range(row0, row0 + nrows):
+            assert (b, g, r) not in seen
+            seen.add((b, g, r))
+        i_first = L - n + row0 // G
+        i_last = L - n + (row0 + nrows - 1) // G
+        assert khi == i_last + 1
+        assert klo == (max(0, i_first - w.window + 1) if w.window > 0 else 0)
+    expect = {(b, g, r) for b in range(w.batch) for g in range(w.hkv)
+              for r in range(int(w.qo_indptr[b + 1] - w.qo_indptr[b]) * G)}
+    assert seen == expect
+    # segments of each block tile its key range exactly once, in split order
+    by_block = {}
+    for cta, blk, t0, t1, split in segs:
+        by_block.setdefault(blk, []).append((split, t0, t1, cta))
+    for bi, (b, g, row0, nrows, klo, khi, nsplit, prb) in enumerate(blocks):
+        parts = sorted(by_block[bi])
+        assert [p[0] for p in parts] == list(range(nsplit))
+        assert parts[0][1] == klo // tile and parts[-1][2] == (khi - 1) // tile + 1
+        for (s0, a0, b0, _), (s1, a1, b1, _) in zip(parts, parts[1:]):
+            assert b0 == a1
+        assert (prb >= 0) == (nsplit > 1)
+    # CTA loads are balanced (stream-K dealing): max <= mean + slack
+    loads = np.zeros(info["ctas"], np.int64)
+    for cta, blk, t0, t1, split in segs:
+        loads[cta] += t1 - t0
+    assert loads.max() <= int(np.ceil(loads.sum() / info["ctas"])) * 1.25 + 2
+    return info
+
+
+@pytest.mark.parametrize("case", [
+    dict(seq=[37], n=[1], hq=8, hkv=1, P=16, W=0),
+    dict(seq=[500, 9, 2300], n=[8, 1, 3], hq=16, hkv=2, P=128, W=0),
+    dict(seq=[640, 400], n=[8, 8], hq=8, hkv=2, P=16, W=70),
+    dict(seq=[190, 333], n=[5, 1], hq=2, hkv=2, P=1, W=4),
+    dict(seq=[3000], n=[300], hq=64, hkv=4, P=128, W=0),
+    dict(seq=[1000, 1000, 1000], n=[1, 8, 1], hq=16, hkv=2, P=128, W=128),
+])
+@pytest.mark.parametrize("num_sms", [1, 7, 152])
+def test_schedule_covers_every_key_once(case, num_sms):
+    w = W.make_workload(0, case["seq"], case["n"], hq=case["hq"], hkv=case["hkv"],
+                        page_size=case["P"], window=case["W"])
+    _coverage_check(w, num_sms)
+
+
+def test_named_configs_schedule_shape():
+    # shapes of the named workloads, without drawing their values
+    for name, seq, n, hq, hkv, P, Wn, rows in [
+        ("decode", [1024 + 37 * i for i in range(32)], [1] * 32, 16, 2, 128, 0, 16),
+        ("verify", [46008] * 4, [8] * 4, 16, 2, 128, 0, 64),
+        ("swa", [8192] * 64, [1, 8] * 32, 16, 2, 128, 128, 64),
+        ("prefill", [30096], [4096], 64, 4, 128, 0, 128),
+    ]:
+        prob, keep = B.make_problem(batch=len(seq), num_q_heads=hq, num_kv_heads=hkv,
+                                    page_size=P, num_pages=9375,
+                                    page_table_stride=max((s + P - 1) // P for s in seq),
+                                    kv_dtype=0, window=Wn, has_sinks=False,
+                                    qo_indptr=np.concatenate([[0], np.cumsum(n)]), seq_lens=seq)
+        plan = B.attn_plan_host(prob, 152, keep)
+        info = B.attn_plan_info(plan)
+        assert info["rows_per_block"] == rows, name
+        assert 0 < info["ctas"] <= 152

@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Tolerances (max-abs / mean-abs on outputs): 2e-2 / 2e-3 with bf16 K/V, 6e-2 /
+6e-3 with fp8 K/V; page-table indexing bit-exact.  The case matrix follows the
+pages' attention tests (decode, 8-token verify, full vs SWA with sinks, ragged
+page boundaries, CUDA graph replay; sglang PR #41886, "Accuracy Tests") and the
+NaN-tail contract (sammysun0711/sglang PR #35).
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+from asymmetric_kv_paged_gb300 import workloads as W
+from oracle import oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": (2e-2, 2e-3), "fp8": (6e-2, 6e-3)}
+LSE_TOL = {"bf16": 2e-3, "fp8": 1e-2}
+
+
+def _runner():
+    from asymmetric_kv_paged_gb300.runner import DeviceWorkload
+    return DeviceWorkload
+
+
+def bf16_to_f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def check_rows(w, got_out, got_lse, ref_out, ref_lse, what=""):
+    mx, mean = TOL[w.kv_dtype]
+    assert np.all(np.isfinite(got_out)), f"{what}: non-finite output"
+    err = np.abs(got_out - ref_out)
+    assert err.max() <= mx, f"{what}: max abs err {err.max():.4g} > {mx}"
+    assert err.mean() <= mean, f"{what}: mean abs err {err.mean():.4g} > {mean}"
+    if got_lse is not None:
+        lerr = np.abs(got_lse - ref_lse)
+        assert lerr.max() <= LSE_TOL[w.kv_dtype] * max(1.0, np.abs(ref_lse).max()), \
+            f"{what}: lse err {lerr.max():.4g}"
+
+
+def run_and_check(w, rows=None):
+    dw = _runner()(w)
+    dw.run()
+    torch.cuda.synchronize()
+    out = bf16_to_f64(dw.out).reshape(-1, W.DV)
+    lse = dw.lse.cpu().numpy().astype(np.float64).reshape(-1)
+    if rows is None:
+        ref_out, ref_lse = oracle.attn_paged(w.host_arrays())
+        ref_out = ref_out.reshape(-1, W.DV)
+        ref_lse = ref_lse.reshape(-1)
+        check_rows(w, out, lse, ref_out, ref_lse, w.name)
+    else:
+        ref_out, ref_lse = oracle.attn_paged(w.host_arrays(), rows=rows)
+        check_rows(w, out[rows], lse[rows], ref_out, ref_lse, w.name)
+    assert B_err(dw) == 0
+    return dw
+
+
+def B_err(dw):
+    from asymmetric_kv_paged_gb300 import binding as B
+    return B.attn_get_device_error(dw.plan)
+
+
+SMALL = [
+    # name, seq_lens, n, hq, hkv, P, window, sinks, kv
+    ("decode_g8_p16", [512], [1], 8, 1, 16, 0, False, "bf16"),
+    ("decode_ragged_p128", [1000, 129, 3000, 64, 700], [1] * 5, 16, 2, 128, 0, False, "bf16"),
+    ("decode_ragged_p3", [50, 333, 1], [1, 1, 1], 8, 2, 3, 0, False, "bf16"),
+    ("decode_g1", [300, 77], [1, 1], 4, 4, 16, 0, False, "bf16"),
+    ("decode_g16", [900], [1], 16, 1, 128, 0, True, "bf16"),
+    ("verify_p1", [1000, 555], [8, 8], 16, 2, 1, 0, False, "bf16"),
+    ("verify_p128", [2000, 130], [8, 3], 16, 2, 128, 0, False, "bf16"),
+    ("swa_sinks_mixed", [700, 700, 260, 900], [1, 8, 8, 1], 16, 2, 128, 128, True, "bf16"),
+    ("swa_small_window", [400, 90], [8, 2], 8, 2, 16, 5, True, "bf16"),
+    ("window_one", [300], [8], 8, 1, 16, 1, True, "bf16"),
+    ("prefill_g16", [700], [300], 32, 2, 128, 0, False, "bf16"),
+    ("prefill_from_empty", [257], [257], 8, 1, 16, 0, False, "bf16"),
+    ("prefill_swa", [900], [200], 16, 2, 64, 100, True, "bf16"),
+    ("empty_requests", [100, 50, 20], [3, 0, 1], 8, 2, 16, 0, False, "bf16"),
+    ("fp8_decode", [2000, 333], [1, 1], 16, 2, 128, 0, False, "fp8"),
+    ("fp8_verify_sinks", [1500, 700], [8, 8], 16, 2, 16, 0, True, "fp8"),
+    ("fp8_prefill", [900], [256], 64, 4, 128, 0, False, "fp8"),
+    ("fp8_swa", [800, 300], [8, 1], 16, 2, 128, 128, True, "fp8"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_parity_small(case):
+    name, seq, n, hq, hkv, P, win, sinks, kv = case
+    w = W.make_workload(zlib.crc32(name.encode()) % 1000, seq, n, hq=hq, hkv=hkv, page_size=P, window=win,
+                        sinks=sinks, kv_dtype=kv, name=name)
+    run_and_check(w)
+
+
+@pytest.mark.parametrize("P", [1, 16, 128])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_v_path_bit_exact(P, kv):
+    """window 1 with n = L: every row sees only its own key, p = 2^0 = 1 exactly,
+    so the output is that key's V row converted to bf16 without rounding."""
+    L = 300
+    w = W.make_workload(7, [L], [L], hq=4, hkv=2, page_size=P, window=1, kv_dtype=kv)
+    w.v_scale = 1.0
+    dw = _runner()(w)
+    dw.run()
+    torch.cuda.synchronize()
+    got = dw.out.view(torch.int16).cpu().numpy().view(np.uint16)      # [L, hq, 128]
+    t = np.arange(L)
+    slots = w.page_table[0, t // P].astype(np.int64) * P + t % P
+    vc = w.v_cache.reshape(-1, w.hkv, W.DV)[slots]                      # [L, hkv, 128]
+    if kv == "bf16":
+        expect = vc
+    else:
+        f = torch.from_numpy(vc.copy()).view(torch.float8_e4m3fn).to(torch.bfloat16)
+        expect = f.view(torch.int16).numpy().view(np.uint16)
+    G = w.hq // w.hkv
+    for h in range(w.hq):
+        assert np.array_equal(got[:, h], expect[:, h // G]), f"head {h}"
+
+
+def test_repeat_runs_bit_identical():
+    w = W.make_workload(8, [3000, 1200], [8, 1], hq=16, hkv=2, page_size=128, sinks=True)
+    dw = _runner()(w)
+    dw.run()
+    a = dw.out.clone()
+    dw.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a, dw.out)
+
+
+def test_graph_replay_bit_identical():
+    """attn_run_paged allocates and synchronises nothing, so it can be captured."""
+    w = W.make_workload(9, [2500, 700, 64], [8, 1, 8], hq=16, hkv=2, page_size=128, window=128,
+                        sinks=True)
+    dw = _runner()(w)
+    dw.run()
+    torch.cuda.synchronize()
+    eager = dw.out.clone()
+    eager_lse = dw.lse.clone()
+    dw.out.zero_()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dw.run(stream=s)
+    for _ in range(3):
+        dw.out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager, dw.out) and torch.equal(eager_lse, dw.lse)
+
+
+def test_run_argument_errors():
+    from asymmetric_kv_paged_gb300 import binding as B
+    w = W.make_workload(10, [500, 300], [8, 1], hq=16, hkv=2, page_size=16, window=64,
+                        sinks=True)
+    dw = _runner()(w)
+    base = dict(plan=dw.plan, q=dw.q, k_cache=dw.k_cache, v_cache=dw.v_cache,
+                page_table=dw.page_table, seq_lens=dw.seq_lens, qo_indptr=dw.qo_indptr,
+                sinks=dw.sinks, window=64, softmax_scale=w.softmax_scale, k_scale=1.0,
+                v_scale=1.0, out=dw.out, lse_out=dw.lse, workspace=dw.workspace)
+    for upd, status in [(dict(window=65), B.ATTN_ERR_INVALID_ARG),
+                        (dict(sinks=None), B.ATTN_ERR_INVALID_ARG),
+                        (dict(q=None), B.ATTN_ERR_INVALID_ARG),
+                        (dict(softmax_scale=float("nan")), B.ATTN_ERR_INVALID_ARG)]:
+        with pytest.raises(B.AttnError) as e:
+            B.attn_run_paged(**dict(base, **upd))
+        assert e.value.status == status
+    if dw.plan.workspace_bytes > 0:
+        small = torch.empty(dw.plan.workspace_bytes - 1, dtype=torch.uint8, device="cuda")
+        with pytest.raises(B.AttnError) as e:
+            B.attn_run_paged(**dict(base, workspace=small))
+        assert e.value.status == B.ATTN_ERR_WORKSPACE
+    B.attn_run_paged(**base)
+    torch.cuda.synchronize()
+
+
+def test_bad_page_id_sets_error_word():
+    """A page id outside the pool is never dereferenced: its rows read as zero and
+    the plan's device error word records it."""
+    from asymmetric_kv_paged_gb300 import binding as B
+    w = W.make_workload(12, [200], [1], hq=8, hkv=1, page_size=16)
+    w.page_table = w.page_table.copy()
+    w.page_table[0, 3] = w.num_pages + 5
+    dw = _runner()(w)
+    dw.run()
+    torch.cuda.synchronize()
+    assert B.attn_get_device_error(dw.plan) & 1
+    assert B.attn_get_device_error(dw.plan) == 0     # read-and-clear
+    assert torch.isfinite(dw.out.float()).all()
+
+
+# ---- full-size workloads, in the benchmark's launch configuration ----
+
+def sampled_rows(w, count, seed):
+    rng = np.random.default_rng(seed)
+    n = w.total_q * w.hq
+    rows = rng.choice(n, size=min(count, n), replace=False)
+    # always include the first and last rows (ragged edges)
+    return np.unique(np.concatenate([rows, [0, n - 1]]))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", list(W.CONFIG_NAMES))
+def test_parity_named_config(name):
+    w = W.named(name)
+    if name == "c1_tiny_decode":
+        run_and_check(w)
+    else:
+        count = {"c5_chunked_prefill": 96}.get(name, 128)
+        run_and_check(w, rows=sampled_rows(w, count, seed=zlib.crc32(name.encode()) % 1000))
