@@ -22,7 +22,7 @@ ATTN_KV_FP8_E4M3 = 1
 
 EXPORTED = ("attn_plan", "attn_run_paged", "attn_run_phase", "attn_plan_destroy", "attn_get_device_error",
             "attn_status_string", "attn_plan_host", "attn_plan_info", "attn_plan_blocks",
-            "attn_plan_segments")
+            "attn_plan_segments", "attn_debug_tc_gemm")
 
 
 class attn_problem_t(ctypes.Structure):
@@ -72,6 +72,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_plan_info.argtypes = [vp, i32p]
     L.attn_plan_blocks.argtypes = [vp, i32p]
     L.attn_plan_segments.argtypes = [vp, i32p]
+    L.attn_debug_tc_gemm.argtypes = [ctypes.c_int32] * 4 + [vp, vp, vp, vp, vp]
     for name in EXPORTED:
         if name != "attn_status_string":
             getattr(L, name).restype = ctypes.c_int
@@ -213,3 +214,14 @@ def attn_plan_segments(plan: Plan):
                                      arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
            "attn_plan_segments")
     return arr[:n]
+
+
+def attn_debug_tc_gemm(mode: int, variant: int, ab_type: int, n: int, a, b, d, status,
+                       stream=None) -> None:
+    """Tensor-core building-block self test (include/attn_paged_debug.h)."""
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    _check(load().attn_debug_tc_gemm(int(mode), int(variant), int(ab_type), int(n), _ptr(a),
+                                     _ptr(b), _ptr(d), _ptr(status), ctypes.c_void_p(int(stream))),
+           "attn_debug_tc_gemm")

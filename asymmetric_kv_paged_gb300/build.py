@@ -19,8 +19,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "split_kv.cu", "merge.cu", "planner.cpp"]
-HEADERS = ["plan.hpp", "kernels.hpp"]
+SOURCES = ["api.cu", "split_kv.cu", "prefill_tc.cu", "merge.cu", "tc_selftest.cu", "planner.cpp"]
+HEADERS = ["plan.hpp", "kernels.hpp", "tc_common.cuh"]
 
 
 def build_dir() -> str:
@@ -40,7 +40,8 @@ def _nvcc() -> str:
 
 def _inputs_mtime() -> float:
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    files += [os.path.join(INCLUDE, "attn_paged.h"), os.path.abspath(__file__)]
+    files += [os.path.join(INCLUDE, h) for h in os.listdir(INCLUDE) if h.endswith(".h")]
+    files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 
 

@@ -2,6 +2,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -100,6 +101,10 @@ attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *
   attn_status_t st = attn_plan_host(problem, num_sms, &p);
   if (st != ATTN_OK) return st;
   p->device = device;
+  {
+    const char *env = std::getenv("AKP_PREFILL_KERNEL");  // development switch
+    p->host.use_tc = env && std::strcmp(env, "tc") == 0;
+  }
   st = upload(p);
   if (st != ATTN_OK) {
     delete p;

@@ -32,5 +32,8 @@ cudaError_t launch_split_kv(const HostPlan &hp, const RunArgs &a, cudaStream_t s
 cudaError_t launch_merge(const HostPlan &hp, const RunArgs &a, cudaStream_t stream);
 // One-time per-device kernel attributes (dynamic shared memory limits).
 cudaError_t prepare_kernels(const HostPlan &hp);
+// Tensor-core (tcgen05) kernel for 128-row blocks.
+cudaError_t launch_prefill_tc(const HostPlan &hp, const RunArgs &a, cudaStream_t stream);
+cudaError_t prepare_prefill_tc(const HostPlan &hp);
 
 }  // namespace akp

@@ -56,6 +56,7 @@ struct HostPlan {
   int64_t part_rows = 0;
   size_t workspace_bytes = 0;
   int32_t multi_split_blocks = 0;
+  bool use_tc = false;           // 128-row blocks on the tcgen05 kernel
 };
 
 // Device-side copy of a plan (owned by attn_plan_s).

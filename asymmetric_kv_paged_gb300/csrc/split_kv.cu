@@ -545,6 +545,7 @@ cudaError_t launch_split_kv(const HostPlan &hp, const RunArgs &a, cudaStream_t s
     case Shape::kRows64:
       return fp8 ? launch_one<4, 1, true>(hp, a, stream) : launch_one<4, 1, false>(hp, a, stream);
     case Shape::kRows128:
+      if (hp.use_tc) return launch_prefill_tc(hp, a, stream);
       return fp8 ? launch_one<8, 1, true>(hp, a, stream) : launch_one<8, 1, false>(hp, a, stream);
   }
   return cudaErrorInvalidValue;
@@ -558,6 +559,7 @@ cudaError_t prepare_kernels(const HostPlan &hp) {
     case Shape::kRows64:
       return fp8 ? prepare_one<4, 1, true>() : prepare_one<4, 1, false>();
     case Shape::kRows128:
+      if (hp.use_tc) return prepare_prefill_tc(hp);
       return fp8 ? prepare_one<8, 1, true>() : prepare_one<8, 1, false>();
   }
   return cudaErrorInvalidValue;

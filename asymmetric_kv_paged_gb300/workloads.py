@@ -231,6 +231,19 @@ def batched_decode() -> Workload:
                          rng=rng)
 
 
+def batched_decode_small() -> Workload:
+    """The batched decode shape at a profiler-friendly size: 32 requests, L ~
+    U[1024, 8192] not page aligned, 16/2 heads, page 128, 2,000-page pool
+    (~190 MB of K/V per step, still larger than L2)."""
+    rng = np.random.default_rng(1012)
+    seq = rng.integers(1024, 8192, size=32, endpoint=True)
+    for i in range(seq.size):
+        while seq[i] % 128 == 0:
+            seq[i] = rng.integers(1024, 8192, endpoint=True)
+    return make_workload(0, seq, np.ones(32, np.int64), hq=16, hkv=2, page_size=128,
+                         num_pages=2000, k_std=0.5, name="c2_batched_decode_small", rng=rng)
+
+
 def verify(page_size: int) -> Workload:
     """4 requests x 8 causal draft tokens over a 46,000-token prefix, 16/2 heads."""
     rng = np.random.default_rng(1003)
@@ -263,6 +276,7 @@ def named(name: str) -> Workload:
     return {
         "c1_tiny_decode": tiny_decode,
         "c2_batched_decode": batched_decode,
+        "c2_batched_decode_small": batched_decode_small,
         "c3a_verify_p128": lambda: verify(128),
         "c3b_verify_p1": lambda: verify(1),
         "c4_swa_sinks": swa_sinks,

@@ -1,0 +1,39 @@
+/*
+ * attn_paged_debug.h - test entry points of libattn_paged.so.
+ *
+ * Not needed to run attention; they expose building blocks of the kernels so
+ * that tests can check them in isolation.  Same status codes as attn_paged.h.
+ */
+#ifndef ATTN_PAGED_DEBUG_H
+#define ATTN_PAGED_DEBUG_H
+
+#include "attn_paged.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * One tensor-core product on one CTA with the shared-memory layouts of the
+ * tensor-core attention kernel (128-byte swizzled operands, accumulator in
+ * tensor memory, fp32 result):
+ *   mode 0: d[128 x n] = a[128 x 192] * b[n x 192]^T, n in {64, 128}
+ *           (both operands K-major, as Q and K in Q.K^T);
+ *   mode 1: d[128 x 128] = a[128 x 64] * b[64 x 128]
+ *           (b stored row-major, i.e. MN-major, as V in P.V); variant 0/1
+ *           picks which descriptor offset spans the two 64-wide column blocks
+ *           of b (0: leading offset, 1: stride offset).
+ * a, b: device 16-bit matrices, row-major (ab_type 0 = fp16, 1 = bf16);
+ * d: device fp32, row-major; status: device int32, set to 1 if the
+ * completion wait timed out (left untouched otherwise).  Asynchronous on
+ * `stream`.  Errors: INVALID_ARG, CUDA.
+ */
+attn_status_t attn_debug_tc_gemm(int32_t mode, int32_t variant, int32_t ab_type, int32_t n,
+                                 const void *a, const void *b, float *d, int32_t *status,
+                                 void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_PAGED_DEBUG_H */

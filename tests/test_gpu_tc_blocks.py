@@ -1,0 +1,46 @@
+"""tcgen05 building blocks in isolation: 128-byte swizzled K-major / MN-major
+shared-memory operands, instruction descriptors, tensor-memory accumulators.
+Compared with a plain fp32 PyTorch product of the same operands."""
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _run(mode, variant, ab_type, n, a, b):
+    from asymmetric_kv_paged_gb300 import binding as B
+    rows, cols = 128, (n if mode == 0 else 128)
+    d = torch.full((rows, cols), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.attn_debug_tc_gemm(mode, variant, ab_type, n, a, b, d, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "tensor-core completion wait timed out"
+    return d
+
+
+@pytest.mark.parametrize("ab_type", [0, 1], ids=["fp16", "bf16"])
+@pytest.mark.parametrize("n", [64, 128])
+def test_qk_shape_kmajor(ab_type, n):
+    g = torch.Generator(device="cuda").manual_seed(1)
+    dt = torch.float16 if ab_type == 0 else torch.bfloat16
+    a = torch.randn(128, 192, device="cuda", generator=g).to(dt)
+    b = torch.randn(n, 192, device="cuda", generator=g).to(dt)
+    d = _run(0, 0, ab_type, n, a, b)
+    ref = a.float() @ b.float().T
+    err = (d - ref).abs().max().item()
+    assert err < 1e-3 * ref.abs().max().item(), err
+
+
+@pytest.mark.parametrize("ab_type", [0, 1], ids=["fp16", "bf16"])
+def test_pv_shape_mnmajor(ab_type):
+    g = torch.Generator(device="cuda").manual_seed(2)
+    dt = torch.float16 if ab_type == 0 else torch.bfloat16
+    a = torch.rand(128, 64, device="cuda", generator=g).to(dt)
+    b = torch.randn(64, 128, device="cuda", generator=g).to(dt)
+    ref = a.float() @ b.float()
+    errs = []
+    for variant in (0, 1):
+        d = _run(1, variant, ab_type, 64, a, b)
+        errs.append((d - ref).abs().max().item())
+    tol = 1e-3 * ref.abs().max().item()
+    assert errs[0] < tol, f"leading-offset variant err {errs[0]:.3g}, stride variant {errs[1]:.3g}"
