@@ -1,8 +1,9 @@
 // C ABI of the paged-attention library (declared in include/attn_paged.h).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
-#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -25,6 +26,41 @@ struct DeviceGuard {
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// cuTensorMapEncodeTiled from the driver, reached through the runtime so the
+// library does not link libcuda directly.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// K (d = 192) or V (d = 128) cache as a 3D tensor [slots][Hkv][d]; boxes of
+// `rows` consecutive slots of one head: 64 bf16 columns with 128-byte swizzle
+// (the tensor-core operand layout), or whole raw E4M3 rows without swizzle.
+bool make_cache_map(CUtensorMap *map, const void *base, bool fp8, int d, int hkv, int64_t slots,
+                    int rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t es = fp8 ? 1 : 2;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)slots};
+  const cuuint64_t strides[2] = {d * es, (cuuint64_t)hkv * d * es};
+  const cuuint32_t box[3] = {fp8 ? (cuuint32_t)d : 64u, 1u, (cuuint32_t)rows};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 void free_device(attn_plan_s *p) {
   if (p->dev.blocks) cudaFree(p->dev.blocks);
@@ -60,7 +96,7 @@ attn_status_t upload(attn_plan_s *p) {
     e = cudaMemcpy(p->dev.merge_items, hp.merge_items.data(),
                    hp.merge_items.size() * sizeof(akp::MergeItem), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(p->dev.err, 0, e_bytes);
-  if (e == cudaSuccess) e = akp::prepare_kernels(hp);
+  if (e == cudaSuccess) e = akp::prepare_attn_tc(hp);
   if (e != cudaSuccess) {
     free_device(p);
     return ATTN_ERR_CUDA;
@@ -83,6 +119,7 @@ attn_status_t attn_plan_host(const attn_problem_t *problem, int32_t num_sms, att
     delete p;
     return st;
   }
+  p->host.use_tma = akp::tc_tma_page_size(problem->page_size, problem->num_pages);
   *plan = p;
   return ATTN_OK;
 }
@@ -101,10 +138,6 @@ attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *
   attn_status_t st = attn_plan_host(problem, num_sms, &p);
   if (st != ATTN_OK) return st;
   p->device = device;
-  {
-    const char *env = std::getenv("AKP_PREFILL_KERNEL");  // development switch
-    p->host.use_tc = env && std::strcmp(env, "tc") == 0;
-  }
   st = upload(p);
   if (st != ATTN_OK) {
     delete p;
@@ -174,12 +207,22 @@ static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const
   a.window = pr.window;
   a.err = plan->dev.err;
 
+  akp::TmaMaps maps{};
+  if ((phases & 1) && hp.use_tma) {
+    if ((reinterpret_cast<uintptr_t>(k_cache) & 15) || (reinterpret_cast<uintptr_t>(v_cache) & 15))
+      return ATTN_ERR_INVALID_ARG;
+    const int64_t slots = (int64_t)pr.num_pages * pr.page_size;
+    const int rows = pr.page_size >= akp::kKeyTile ? akp::kKeyTile : pr.page_size;
+    if (!make_cache_map(&maps.k, k_cache, fp8, akp::kDqk, pr.num_kv_heads, slots, rows) ||
+        !make_cache_map(&maps.v, v_cache, fp8, akp::kDv, pr.num_kv_heads, slots, rows))
+      return ATTN_ERR_CUDA;
+  }
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return ATTN_ERR_CUDA;
   DeviceGuard guard(cur == plan->device ? cur : plan->device);
   if (!guard.ok) return ATTN_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if ((phases & 1) && akp::launch_split_kv(hp, a, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  if ((phases & 1) && akp::launch_attn_tc(hp, a, maps, st) != cudaSuccess) return ATTN_ERR_CUDA;
   if ((phases & 2) && akp::launch_merge(hp, a, st) != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
@@ -238,7 +281,7 @@ attn_status_t attn_plan_info(attn_plan_t plan, int32_t info[8]) {
   info[0] = (int32_t)hp.blocks.size();
   info[1] = (int32_t)hp.segs.size();
   info[2] = hp.num_ctas;
-  info[3] = (int32_t)hp.shape;
+  info[3] = akp::kBlockRows;
   info[4] = akp::kKeyTile;
   info[5] = hp.multi_split_blocks;
   info[6] = (int32_t)(hp.workspace_bytes & 0x7FFFFFFF);

@@ -1,0 +1,650 @@
+// Split-KV paged attention on the Blackwell tensor-core path (tcgen05 + TMEM),
+// for every mode: decode, multi-token verify and chunked prefill.
+//
+// A CTA walks the key tiles (64 keys) of its work segments.  Each segment
+// belongs to one row block: up to 128 query rows of one (request, KV head),
+// row r <-> (token r / G, head g*G + r % G), so every draft token and every
+// head of the group shares one pass over the keys ("one program per whole
+// verify", and the 8-token x 16-head packing of the prefill kernel on the
+// MiMo-V2.6-Flash-RL model card, "What the kernels do").  Blocks with fewer
+// than 128 rows (decode: G rows) still issue M=128 MMAs: the tensor pipe has
+// time to spare while the tile streams in from HBM.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax + epilogue: thread r owns row r (= TMEM lane r);
+//   warps 4-7  converters: stage Q per block; turn raw FP8 K/V tiles into
+//              exact fp16 operand tiles; zero V rows of keys outside the
+//              block's range on edge tiles (unused slots may hold NaN:
+//              sammysun0711/sglang PR #35, FlyPA V-tail masking); or, for
+//              page sizes TMA cannot tile, gather K/V rows themselves;
+//   warp  8    TMEM allocation and every tcgen05.mma (one thread);
+//   warp  9    TMA producer: page-table lookup, then 3D tensor-map loads of
+//              the K/V boxes (BF16: straight into the 128-byte swizzled
+//              operand layout; FP8: raw rows into a staging ring).
+// TMEM: S double buffer (2 x 64 columns) + O (128 columns).
+// Every wait is bounded in time; a broken invariant ends the kernel with bit 1
+// of the plan's error word set instead of hanging the GPU.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "kernels.hpp"
+#include "tc_common.cuh"
+
+namespace akp {
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kN = kKeyTile;                 // keys per tile (64)
+constexpr int kThreads = 10 * 32;
+constexpr int kBlk = kN * 128;               // one 64-column block of a 64-row tile: 8 KB
+constexpr int kQBlock = kRows * 128;         // one 64-column block of Q: 16 KB
+constexpr int kQBytes = 3 * kQBlock;         // 48 KB
+constexpr int kOpK = 3 * kBlk;               // K operand tile: 24 KB
+constexpr int kOpBytes = kOpK + 2 * kBlk;    // + V operand tile: 40 KB
+constexpr int kRawK = kN * kDqk;             // raw E4M3 K rows: 12 KB
+constexpr int kRawBytes = kRawK + kN * kDv;  // + raw V rows: 20 KB
+constexpr int kPBytes = kRows * 128;         // P tile [128 rows x 64 keys]: 16 KB
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemO = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;    // base-2 growth allowed before O is rescaled
+
+template <bool FP8>
+struct Layout {
+  static constexpr int kOpStages = FP8 ? 2 : 3;
+  static constexpr int kRawStages = FP8 ? 3 : 0;
+  static constexpr int kOffOp = kQBytes;
+  static constexpr int kOffRaw = kOffOp + kOpStages * kOpBytes;
+  static constexpr int kOffP = kOffRaw + kRawStages * kRawBytes;
+  static constexpr int kUsed = kOffP + 2 * kPBytes;
+  static constexpr int kSmem = kUsed + 1024;  // room to align the base to 1024 B
+  static constexpr int kTmaStages = FP8 ? kRawStages : kOpStages;
+};
+
+struct Bars {
+  uint64_t tma_full[3], tma_empty[3];
+  uint64_t op_full[3], op_empty[3];
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full[2], pv_done[2];
+  uint64_t o_free, final_done;
+};
+
+// Walks the CTA's tiles in order: segment, tile id, first/last flags.
+struct Cursor {
+  const SegDesc *segs;
+  int seg, seg_end, tile, si;
+  __device__ void init(const SegDesc *s, int b, int e) {
+    segs = s;
+    seg = b;
+    seg_end = e;
+    tile = s[b].tile_begin;
+    si = 0;
+  }
+  __device__ bool first() const { return tile == segs[seg].tile_begin; }
+  __device__ bool last() const { return tile + 1 == segs[seg].tile_end; }
+  __device__ void next() {
+    if (++tile == segs[seg].tile_end && seg + 1 < seg_end) {
+      ++seg;
+      ++si;
+      tile = segs[seg].tile_begin;
+    }
+  }
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t cvt_pair(float lo, float hi, bool half) {
+  if (half) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 16 E4M3 codes -> 16 fp16 values (exact), as two 16-byte chunks.
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 raw, uint4 &lo, uint4 &hi) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[q] & 0xFFFFu),
+                                               __NV_E4M3);
+    __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[q] >> 16),
+                                               __NV_E4M3);
+    h[2 * q] = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
+    h[2 * q + 1] = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
+  }
+  lo = make_uint4(h[0], h[1], h[2], h[3]);
+  hi = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&w[q]);
+    __half2 h = __float22half2_rn(__bfloat1622float2(b));
+    w[q] = *reinterpret_cast<uint32_t *>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(tc::smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+template <bool FP8, bool TMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const RunArgs a, const __grid_constant__ TmaMaps maps) {
+  using Lay = Layout<FP8>;
+  constexpr int NS = Lay::kOpStages;
+  constexpr int NT = Lay::kTmaStages;
+  constexpr bool kHalf = FP8;  // operand type: fp16 for FP8 caches, bf16 otherwise
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
+  __shared__ Bars bars;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int seg_begin = a.cta_seg_begin[blockIdx.x];
+  const int seg_end = a.cta_seg_begin[blockIdx.x + 1];
+  if (seg_begin >= seg_end) return;
+  int total = 0;
+  for (int s = seg_begin; s < seg_end; ++s) total += a.segs[s].tile_end - a.segs[s].tile_begin;
+
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < 3; ++s) {
+      tc::mbar_init(&bars.tma_full[s], 1);
+      tc::mbar_init(&bars.tma_empty[s], 128);
+      tc::mbar_init(&bars.op_full[s], 128);
+      tc::mbar_init(&bars.op_empty[s], 1);
+    }
+    tc::mbar_init(&bars.q_full, 128);
+    tc::mbar_init(&bars.q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bars.s_full[b], 1);
+      tc::mbar_init(&bars.s_empty[b], 128);
+      tc::mbar_init(&bars.p_full[b], 128);
+      tc::mbar_init(&bars.pv_done[b], 1);
+    }
+    tc::mbar_init(&bars.o_free, 128);
+    tc::mbar_init(&bars.final_done, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 8) tc::tmem_alloc(&tmem_slot, kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t sbase = tc::smem_u32(smem);
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ TMA producer
+    if (TMA && (tid & 31) == 0) {
+      const int box = a.page_size >= kN ? kN : a.page_size;   // key rows per box
+      const int nbox = kN / box;
+      const int oob = a.num_pages * a.page_size;              // first slot past the pool
+      constexpr uint32_t kTileBytes = FP8 ? kRawBytes : kOpBytes;
+      Cursor cur;
+      cur.init(a.segs, seg_begin, seg_end);
+      for (int k = 0; k < total; ++k, cur.next()) {
+        const int t = k % NT;
+        uint64_t *empty = FP8 ? &bars.tma_empty[t] : &bars.op_empty[t];
+        if (k >= NT && !tc::mbar_wait(empty, ((k / NT) - 1) & 1, &abort_flag)) break;
+        const BlockDesc bd = a.blocks[a.segs[cur.seg].block];
+        const int32_t *pt_row = a.page_table + (int64_t)bd.b * a.pt_stride;
+        const int key0 = cur.tile * kN;
+        mbar_expect_tx(&bars.tma_full[t], kTileBytes);
+        const uint32_t dst = sbase + (FP8 ? Lay::kOffRaw + t * kRawBytes : Lay::kOffOp + t * kOpBytes);
+        for (int i = 0; i < nbox; ++i) {
+          const int j = key0 + i * box;
+          int slot = oob;  // boxes with no visible key read past the pool: zero fill
+          if (j + box > bd.klo && j < bd.khi) {
+            const int32_t page = __ldg(pt_row + j / a.page_size);
+            if (page >= 0 && page < a.num_pages)
+              slot = page * a.page_size + j % a.page_size;
+            else
+              atomicOr(a.err, 1);
+          }
+          if (FP8) {
+            tma_load_3d(dst + i * box * kDqk, &maps.k, 0, bd.g, slot, &bars.tma_full[t]);
+            tma_load_3d(dst + kRawK + i * box * kDv, &maps.v, 0, bd.g, slot, &bars.tma_full[t]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 3; ++c)
+              tma_load_3d(dst + c * kBlk + i * box * 128, &maps.k, 64 * c, bd.g, slot,
+                          &bars.tma_full[t]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d(dst + kOpK + c * kBlk + i * box * 128, &maps.v, 64 * c, bd.g, slot,
+                          &bars.tma_full[t]);
+          }
+        }
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ converters
+    const int ct = tid - 128;
+    const uint8_t *kc = static_cast<const uint8_t *>(a.k_cache);
+    const uint8_t *vc = static_cast<const uint8_t *>(a.v_cache);
+    Cursor cur;
+    cur.init(a.segs, seg_begin, seg_end);
+    for (int k = 0; k < total; ++k, cur.next()) {
+      const SegDesc sd = a.segs[cur.seg];
+      const BlockDesc bd = a.blocks[sd.block];
+      if (cur.first()) {
+        if (cur.si > 0 && !tc::mbar_wait(&bars.q_empty, (cur.si - 1) & 1, &abort_flag)) break;
+        for (int idx = ct; idx < kRows * 24; idx += 128) {
+          const int r = idx / 24;
+          const int ch = idx % 24;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (r < bd.nrows) {
+            const int flat = bd.row0 + r;
+            const int tok = bd.tok0 + flat / a.group;
+            const int h = bd.g * a.group + flat % a.group;
+            v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) +
+                                                      ((int64_t)tok * a.hq + h) * kDqk) + ch);
+            if (kHalf) v = bf16x8_to_f16x8(v);
+          }
+          *reinterpret_cast<uint4 *>(smem + (ch >> 3) * kQBlock + tc::sw128_offset(r, ch & 7)) = v;
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&bars.q_full);
+      }
+      const int s = k % NS;
+      const int key0 = cur.tile * kN;
+      uint8_t *op = smem + Lay::kOffOp + s * kOpBytes;
+      if (TMA && !FP8) {
+        // BF16 tile landed by TMA in operand layout; zero V rows outside the range
+        if (!tc::mbar_wait(&bars.tma_full[s], (k / NS) & 1, &abort_flag)) break;
+        if (key0 < bd.klo || key0 + kN > bd.khi) {
+          for (int idx = ct; idx < kN * 16; idx += 128) {
+            const int kk = idx >> 4;
+            const int j = key0 + kk;
+            if (j < bd.klo || j >= bd.khi) {
+              const int c = (idx >> 3) & 1;
+              *reinterpret_cast<uint4 *>(op + kOpK + c * kBlk + tc::sw128_offset(kk, idx & 7)) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&bars.op_full[s]);
+        continue;
+      }
+      if (k >= NS && !tc::mbar_wait(&bars.op_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
+      constexpr int kEs = FP8 ? 1 : 2;
+      constexpr int kKch = kDqk * kEs / 16;  // source 16-byte chunks per K row
+      constexpr int kVch = kDv * kEs / 16;
+      constexpr int kPer = kN * (kKch + kVch) / 128;
+      // chunk u of this thread: (is K, key within the tile, 16-byte chunk of the row)
+      //  TMA staging: consecutive threads take consecutive chunks (conflict-free reads);
+      //  gather: two threads per key, so each thread looks up one page per tile.
+      auto chunk_of = [&](int u, bool &is_k, int &kk, int &ch) {
+        if (TMA) {
+          const int c = ct + u * 128;
+          is_k = c < kN * kKch;
+          const int cc = is_k ? c : c - kN * kKch;
+          const int nch = is_k ? kKch : kVch;
+          kk = cc / nch;
+          ch = cc % nch;
+        } else {
+          kk = ct >> 1;
+          const int part = ct & 1;
+          is_k = u < kKch / 2;
+          ch = is_k ? part * (kKch / 2) + u : part * (kVch / 2) + (u - kKch / 2);
+        }
+      };
+      uint4 buf[kPer];
+      if (TMA) {
+        // FP8 rows staged by TMA: [64 keys x 192 B] K then [64 keys x 128 B] V
+        const int t = k % NT;
+        if (!tc::mbar_wait(&bars.tma_full[t], (k / NT) & 1, &abort_flag)) break;
+        const uint8_t *raw = smem + Lay::kOffRaw + t * kRawBytes;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          bool is_k;
+          int kk, ch;
+          chunk_of(u, is_k, kk, ch);
+          buf[u] = *reinterpret_cast<const uint4 *>(
+              raw + (is_k ? kk * kDqk + ch * 16 : kRawK + kk * kDv + ch * 16));
+        }
+        tc::mbar_arrive(&bars.tma_empty[t]);
+      } else {
+        // gather: the page of this thread's key, then 16-byte loads of its chunks
+        const int j = key0 + (ct >> 1);
+        int64_t slot = -1;
+        if (j >= bd.klo && j < bd.khi) {
+          const int32_t page = __ldg(a.page_table + (int64_t)bd.b * a.pt_stride + j / a.page_size);
+          if (page >= 0 && page < a.num_pages)
+            slot = (int64_t)page * a.page_size + j % a.page_size;
+          else
+            atomicOr(a.err, 1);
+        }
+        const int64_t srow = (slot >= 0 ? slot : 0) * a.hkv + bd.g;
+        const uint4 *krow = reinterpret_cast<const uint4 *>(kc + srow * (kDqk * kEs));
+        const uint4 *vrow = reinterpret_cast<const uint4 *>(vc + srow * (kDv * kEs));
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          bool is_k;
+          int kk, ch;
+          chunk_of(u, is_k, kk, ch);
+          buf[u] = slot >= 0 ? __ldg((is_k ? krow : vrow) + ch) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        bool is_k;
+        int kk, ch;
+        chunk_of(u, is_k, kk, ch);
+        const int j = key0 + kk;
+        const bool keep = j >= bd.klo && j < bd.khi;
+        uint8_t *dst = op + (is_k ? 0 : kOpK);
+        if (FP8) {
+          uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+          if (keep) e4m3x16_to_f16(buf[u], lo, hi);
+          const int c16 = 2 * ch;
+          *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
+          *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
+                                     tc::sw128_offset(kk, (c16 + 1) & 7)) = hi;
+        } else {
+          *reinterpret_cast<uint4 *>(dst + (ch >> 3) * kBlk + tc::sw128_offset(kk, ch & 7)) =
+              keep ? buf[u] : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars.op_full[s]);
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    if ((tid & 31) == 0) {
+      const uint32_t id_s = tc::idesc_f16(kHalf ? 0 : 1, 0, 0, kRows, kN);
+      const uint32_t id_pv = tc::idesc_f16(kHalf ? 0 : 1, 0, 1, kRows, kDv);
+      Cursor cs, cp;
+      cs.init(a.segs, seg_begin, seg_end);
+      cp.init(a.segs, seg_begin, seg_end);
+      bool ok = true;
+      auto issue_pv = [&](int k) -> bool {
+        const int b = k & 1;
+        const int s = k % NS;
+        if (!tc::mbar_wait(&bars.p_full[b], (k >> 1) & 1, &abort_flag)) return false;
+        const bool first = cp.first();
+        if (first && cp.si > 0 && !tc::mbar_wait(&bars.o_free, (cp.si - 1) & 1, &abort_flag))
+          return false;
+        tc::tc_fence_after();
+        const uint32_t pb = sbase + Lay::kOffP + b * kPBytes;
+        const uint32_t vb = sbase + Lay::kOffOp + s * kOpBytes + kOpK;
+#pragma unroll
+        for (int kk = 0; kk < kN / 16; ++kk) {
+          const uint64_t ad = tc::smem_desc_sw128(pb + kk * 32, 16, 1024);
+          const uint64_t bdsc = tc::smem_desc_sw128(vb + kk * 16 * 128, kBlk, 1024);
+          tc::mma_f16_ss(tmem + kTmemO, ad, bdsc, id_pv, (!first || kk > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&bars.op_empty[s]);
+        tc::mma_commit(&bars.pv_done[b]);
+        cp.next();
+        return true;
+      };
+      for (int k = 0; k < total && ok; ++k, cs.next()) {
+        const int s = k % NS;
+        const int b = k & 1;
+        if (cs.first() && !tc::mbar_wait(&bars.q_full, cs.si & 1, &abort_flag)) break;
+        if (!tc::mbar_wait(&bars.op_full[s], (k / NS) & 1, &abort_flag)) break;
+        if (k >= 2 && !tc::mbar_wait(&bars.s_empty[b], ((k >> 1) - 1) & 1, &abort_flag)) break;
+        tc::tc_fence_after();
+        const uint32_t kb = sbase + Lay::kOffOp + s * kOpBytes;
+#pragma unroll
+        for (int ks = 0; ks < kDqk / 16; ++ks) {
+          const uint32_t koff = (ks & 3) * 32;
+          const uint64_t ad = tc::smem_desc_sw128(sbase + (ks >> 2) * kQBlock + koff, 16, 1024);
+          const uint64_t bdsc = tc::smem_desc_sw128(kb + (ks >> 2) * kBlk + koff, 16, 1024);
+          tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, ks > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&bars.s_full[b]);
+        if (cs.last()) tc::mma_commit(&bars.q_empty);
+        if (k >= 1) ok = issue_pv(k - 1);
+      }
+      if (ok && !abort_flag) issue_pv(total - 1);
+      tc::mma_commit(&bars.final_done);
+      tc::mbar_wait(&bars.final_done, 0, &abort_flag);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int r = tid;  // query row of the block == TMEM lane
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    Cursor cur;
+    cur.init(a.segs, seg_begin, seg_end);
+    float m_run = -INFINITY, l_run = 0.f;
+    int row_lo = 0, row_hi = 0, tok = 0, h = 0;
+    bool valid = false, warp_live = false;
+    BlockDesc bd{};
+    for (int k = 0; k < total; ++k, cur.next()) {
+      const SegDesc sd = a.segs[cur.seg];
+      const bool first = cur.first();
+      if (first) {
+        bd = a.blocks[sd.block];
+        valid = r < bd.nrows;
+        warp_live = warp * 32 < bd.nrows;
+        row_lo = row_hi = 0;
+        if (valid) {
+          const int flat = bd.row0 + r;
+          const int t = flat / a.group;
+          tok = bd.tok0 + t;
+          h = bd.g * a.group + flat % a.group;
+          const int i = bd.L - bd.n + t;
+          row_hi = i + 1;
+          row_lo = a.window > 0 ? max(0, i - a.window + 1) : 0;
+        }
+      }
+      const int b = k & 1;
+      if (!tc::mbar_wait(&bars.s_full[b], (k >> 1) & 1, &abort_flag)) break;
+      tc::tc_fence_after();
+      float sv[kN];
+      if (warp_live) {
+        uint32_t raw[32];
+        tc::tmem_ld32(tmem + lane_base + b * kN, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
+        tc::tmem_ld32(tmem + lane_base + b * kN + 32, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(raw[j]);
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars.s_empty[b]);
+
+      if (warp_live) {
+        const int key0 = cur.tile * kN;
+        float m_tile = -INFINITY;
+        if (key0 >= row_lo && key0 + kN <= row_hi) {
+#pragma unroll
+          for (int j = 0; j < kN; ++j) {
+            sv[j] *= a.scale_log2;
+            m_tile = fmaxf(m_tile, sv[j]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kN; ++j) {
+            const int key = key0 + j;
+            sv[j] = (key >= row_lo && key < row_hi) ? sv[j] * a.scale_log2 : -INFINITY;
+            m_tile = fmaxf(m_tile, sv[j]);
+          }
+        }
+        if (first) {
+          m_run = m_tile;
+          l_run = 0.f;
+        } else {
+          const bool need = m_tile > m_run + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            if (!tc::mbar_wait(&bars.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, &abort_flag)) break;
+            tc::tc_fence_after();
+            const float m_new = need ? m_tile : m_run;
+            const float alpha = need ? ex2(m_run - m_new) : 1.f;
+#pragma unroll
+            for (int c = 0; c < kDv / 32; ++c) {
+              uint32_t o[32];
+              tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tc::tmem_st32(tmem + lane_base + kTmemO + c * 32, o);
+            }
+            tc::tmem_wait_st();
+            l_run *= alpha;
+            m_run = m_new;
+          }
+        }
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        uint32_t pk[kN / 2];
+        float rs = 0.f;
+#pragma unroll
+        for (int j = 0; j < kN; j += 2) {
+          const float p0 = ex2(sv[j] - m_use);
+          const float p1 = ex2(sv[j + 1] - m_use);
+          rs += p0 + p1;
+          pk[j / 2] = cvt_pair(p0, p1, kHalf);
+        }
+        l_run += rs;
+        if (k >= 2 && !tc::mbar_wait(&bars.pv_done[b], ((k - 2) >> 1) & 1, &abort_flag)) break;
+        uint8_t *pb = smem + Lay::kOffP + b * kPBytes;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4 *>(pb + tc::sw128_offset(r, c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        tc::fence_proxy_async_smem();
+      } else if (k >= 2 && !tc::mbar_wait(&bars.pv_done[b], ((k - 2) >> 1) & 1, &abort_flag)) {
+        break;
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars.p_full[b]);
+
+      if (cur.last()) {
+        if (!tc::mbar_wait(&bars.pv_done[b], (k >> 1) & 1, &abort_flag)) break;
+        tc::tc_fence_after();
+        if (warp_live) {
+          const bool single = bd.num_splits == 1;
+          float scale_o = 0.f, lse = -INFINITY;
+          if (single) {
+            const float sig = (a.sinks && valid) ? a.sinks[h] * kLog2e : -INFINITY;
+            const float MM = fmaxf(m_run, sig);
+            if (MM != -INFINITY) {
+              const float Z = l_run * exp2f(m_run - MM) + exp2f(sig - MM);
+              scale_o = exp2f(m_run - MM) * a.v_scale / Z;
+              lse = (MM + log2f(Z)) * kLn2;
+            }
+          } else {
+            scale_o = l_run > 0.f ? a.v_scale / l_run : 0.f;
+            lse = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+          }
+          const int prow = bd.part_row_base + sd.split * bd.nrows + r;
+#pragma unroll
+          for (int c = 0; c < kDv / 32; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
+            tc::tmem_wait_ld();
+            if (!valid) continue;
+            if (single) {
+              uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) +
+                                                     ((int64_t)tok * a.hq + h) * kDv + c * 32);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  w[e] = cvt_pair(__uint_as_float(o[8 * q + 2 * e]) * scale_o,
+                                  __uint_as_float(o[8 * q + 2 * e + 1]) * scale_o, false);
+                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            } else {
+              float4 *dst = reinterpret_cast<float4 *>(a.part_o + (int64_t)prow * kDv + c * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(o[4 * q]) * scale_o,
+                                     __uint_as_float(o[4 * q + 1]) * scale_o,
+                                     __uint_as_float(o[4 * q + 2]) * scale_o,
+                                     __uint_as_float(o[4 * q + 3]) * scale_o);
+            }
+          }
+          if (valid) {
+            if (single) {
+              if (a.lse_out) a.lse_out[(int64_t)tok * a.hq + h] = lse;
+            } else {
+              a.part_lse[prow] = lse;
+            }
+          }
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars.o_free);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (tid == 0 && abort_flag) atomicOr(a.err, 2);
+  if (warp == 8) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <bool FP8, bool TMA>
+cudaError_t launch_one(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
+  attn_tc_kernel<FP8, TMA><<<hp.num_ctas, kThreads, Layout<FP8>::kSmem, st>>>(a, m);
+  return cudaGetLastError();
+}
+
+template <bool FP8, bool TMA>
+cudaError_t prepare_one() {
+  return cudaFuncSetAttribute(attn_tc_kernel<FP8, TMA>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<FP8>::kSmem);
+}
+
+}  // namespace
+
+bool tc_tma_page_size(int32_t page_size, int32_t num_pages) {
+  if ((int64_t)num_pages * page_size >= INT32_MAX) return false;
+  return page_size % kN == 0 || (kN % page_size == 0 && page_size >= 8);
+}
+
+cudaError_t launch_attn_tc(const HostPlan &hp, const RunArgs &a, const TmaMaps &m,
+                           cudaStream_t stream) {
+  if (hp.num_ctas == 0) return cudaSuccess;
+  const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
+  if (hp.use_tma)
+    return fp8 ? launch_one<true, true>(hp, a, m, stream) : launch_one<false, true>(hp, a, m, stream);
+  return fp8 ? launch_one<true, false>(hp, a, m, stream) : launch_one<false, false>(hp, a, m, stream);
+}
+
+cudaError_t prepare_attn_tc(const HostPlan &hp) {
+  const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
+  if (hp.use_tma) return fp8 ? prepare_one<true, true>() : prepare_one<false, true>();
+  return fp8 ? prepare_one<true, false>() : prepare_one<false, false>();
+}
+
+}  // namespace akp

@@ -1,5 +1,6 @@
 // Kernel launch interfaces (internal).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "plan.hpp"
@@ -26,14 +27,20 @@ struct RunArgs {
   int32_t *err;
 };
 
-// Split-KV attention over the plan's segments (decode, verify and prefill).
-cudaError_t launch_split_kv(const HostPlan &hp, const RunArgs &a, cudaStream_t stream);
+// Tensor maps of the K and V caches as 3D tensors [slots][Hkv][D] (TMA loads).
+struct TmaMaps {
+  CUtensorMap k, v;
+};
+
+// Split-KV attention over the plan's segments (decode, verify and prefill) on
+// the tcgen05 tensor-core path.  `maps` is read only when hp.use_tma.
+cudaError_t launch_attn_tc(const HostPlan &hp, const RunArgs &a, const TmaMaps &maps,
+                           cudaStream_t stream);
+// One-time per-device kernel attributes (dynamic shared memory limits).
+cudaError_t prepare_attn_tc(const HostPlan &hp);
+// Whether K/V tiles of this page size can be loaded as TMA boxes.
+bool tc_tma_page_size(int32_t page_size, int32_t num_pages);
 // Log-sum-exp merge of multi-split blocks.
 cudaError_t launch_merge(const HostPlan &hp, const RunArgs &a, cudaStream_t stream);
-// One-time per-device kernel attributes (dynamic shared memory limits).
-cudaError_t prepare_kernels(const HostPlan &hp);
-// Tensor-core (tcgen05) kernel for 128-row blocks.
-cudaError_t launch_prefill_tc(const HostPlan &hp, const RunArgs &a, cudaStream_t stream);
-cudaError_t prepare_prefill_tc(const HostPlan &hp);
 
 }  // namespace akp

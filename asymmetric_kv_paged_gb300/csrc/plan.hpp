@@ -13,13 +13,10 @@ constexpr int kDqk = 192;       // query/key head dim
 constexpr int kDv = 128;        // value head dim
 constexpr int kKeyTile = 64;    // keys per pipeline tile
 
-// Row-block shapes of the split-KV kernel.  A block packs `rows` query rows of
-// one (request, KV head): row r <-> (token r / G, head g*G + r % G).
-enum class Shape : int32_t {
-  kRows16 = 16,    // decode: 4 warps split each key tile, one 16-row group
-  kRows64 = 64,    // verify: 4 warps x 16 rows, every warp sees the whole tile
-  kRows128 = 128,  // prefill: 8 warps x 16 rows
-};
+// Query rows per row block.  A block packs up to 128 query rows of one
+// (request, KV head): row r <-> (token r / G, head g*G + r % G); decode blocks
+// hold G rows, verify blocks n*G, prefill blocks 128.
+constexpr int32_t kBlockRows = 128;
 
 // One row block: rows [row0, row0 + nrows) of (b, g).  Keys [klo, khi) are
 // the union of what its rows can see.
@@ -46,7 +43,6 @@ struct HostPlan {
   attn_problem_t prob{};
   std::vector<int32_t> qo_indptr, seq_lens;
   int32_t group = 1;             // G = Hq / Hkv
-  Shape shape = Shape::kRows16;
   int32_t num_sms = 0, num_ctas = 0, threads = 0;
   std::vector<BlockDesc> blocks;
   std::vector<SegDesc> segs;
@@ -56,7 +52,7 @@ struct HostPlan {
   int64_t part_rows = 0;
   size_t workspace_bytes = 0;
   int32_t multi_split_blocks = 0;
-  bool use_tc = false;           // 128-row blocks on the tcgen05 kernel
+  bool use_tma = false;          // K/V tiles as TMA boxes (else gathered by threads)
 };
 
 // Device-side copy of a plan (owned by attn_plan_s).

@@ -17,22 +17,6 @@
 
 namespace akp {
 
-namespace {
-
-Shape choose_shape(const HostPlan &hp) {
-  int64_t max_rows = 0;
-  for (int32_t b = 0; b < hp.prob.batch; ++b) {
-    int64_t n = hp.qo_indptr[b + 1] - hp.qo_indptr[b];
-    max_rows = std::max<int64_t>(max_rows, n * hp.group);
-  }
-  if (max_rows <= 16) return Shape::kRows16;
-  if (max_rows <= 64) return Shape::kRows64;
-  return Shape::kRows128;
-}
-
-int32_t threads_for(Shape s) { return s == Shape::kRows128 ? 256 : 128; }
-
-}  // namespace
 
 attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan *out) {
   if (!p || !out || num_sms <= 0) return ATTN_ERR_INVALID_ARG;
@@ -66,9 +50,8 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   if ((int64_t)hp.qo_indptr[p->batch] * p->num_q_heads > INT32_MAX / kDqk)
     return ATTN_ERR_UNSUPPORTED;
 
-  hp.shape = choose_shape(hp);
-  hp.threads = threads_for(hp.shape);
-  const int32_t rows_per_block = (int32_t)hp.shape;
+  hp.threads = 320;
+  const int32_t rows_per_block = kBlockRows;
   const int32_t G = hp.group;
 
   // Row blocks.
