@@ -22,7 +22,7 @@ ATTN_KV_FP8_E4M3 = 1
 
 EXPORTED = ("attn_plan", "attn_run_paged", "attn_run_phase", "attn_plan_destroy", "attn_get_device_error",
             "attn_status_string", "attn_plan_host", "attn_plan_info", "attn_plan_blocks",
-            "attn_plan_segments", "attn_debug_tc_gemm")
+            "attn_plan_segments", "attn_debug_tc_gemm", "attn_run_paged_no_workspace")
 
 
 class attn_problem_t(ctypes.Structure):
@@ -64,6 +64,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_run_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, ctypes.c_float,
                                  ctypes.c_float, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp]
     L.attn_run_phase.argtypes = [vp, ctypes.c_int32] + L.attn_run_paged.argtypes[1:]
+    L.attn_run_paged_no_workspace.argtypes = L.attn_run_paged.argtypes[:14] + [vp]
     L.attn_plan_destroy.argtypes = [vp]
     L.attn_get_device_error.argtypes = [vp, vp, i32p]
     L.attn_status_string.argtypes = [ctypes.c_int]
@@ -179,6 +180,21 @@ def attn_run_phase(plan: Plan, phase: int, q, k_cache, v_cache, page_table, seq_
                      softmax_scale, k_scale, v_scale, out, lse_out, workspace, stream)
     _check(load().attn_run_phase(ctypes.c_void_p(plan.handle), int(phase), *args),
            "attn_run_phase")
+
+
+NO_WORKSPACE_MAX_BYTES = 16 * 1024 * 1024
+
+
+def attn_run_paged_no_workspace(plan: Plan, q, k_cache, v_cache, page_table, seq_lens, qo_indptr,
+                                sinks, window: int, softmax_scale: float, k_scale: float,
+                                v_scale: float, out, lse_out=None, stream=None) -> None:
+    """attn_run_paged on the library's own scratch (no workspace argument), for
+    callers that cannot allocate device memory."""
+    args = _run_args(plan, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks, window,
+                     softmax_scale, k_scale, v_scale, out, lse_out, None, stream)
+    args = args[:13] + args[15:]        # drop the workspace pointer and size
+    _check(load().attn_run_paged_no_workspace(ctypes.c_void_p(plan.handle), *args),
+           "attn_run_paged_no_workspace")
 
 
 def attn_get_device_error(plan: Plan) -> int:

@@ -160,6 +160,43 @@ attn_status_t attn_run_phase(attn_plan_t plan, int32_t phase, const void *q,
                              float *lse_out, void *workspace, size_t workspace_bytes,
                              void *stream);
 
+/*
+ * Size of the library-owned scratch used by attn_run_paged_no_workspace.
+ */
+#define ATTN_NO_WORKSPACE_MAX_BYTES (16u * 1024u * 1024u)
+
+/*
+ * attn_run_paged for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart: this entry point exists for integration.
+ * Some callers have no way to obtain the workspace attn_run_paged asks for:
+ * code that runs while a stream is being captured into a CUDA graph (device
+ * allocation is not permitted during capture), plugins that a host
+ * framework hands tensor pointers but no allocator, and serving loops that
+ * forbid allocation on the hot path.  This call takes the same arguments as
+ * attn_run_paged minus the workspace and uses instead one scratch array of
+ * ATTN_NO_WORKSPACE_MAX_BYTES bytes in device global memory that the library
+ * owns: every GPU that loads the library holds that array until the process
+ * exits.  Nothing is allocated, here or later.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (a host-side query, no allocation); make that first call before
+ *     any stream capture.
+ *   - Plans whose workspace_bytes exceed ATTN_NO_WORKSPACE_MAX_BYTES are
+ *     rejected with ATTN_ERR_WORKSPACE before anything is launched.
+ *   - All calls share the one array, and it keeps whatever the last call left
+ *     in it; nothing in it needs to start at zero, because each call writes
+ *     every partial it later reads.  Calls whose kernels overlap on the GPU
+ *     (different streams, or different threads without ordering) race on the
+ *     array and give wrong results: order them on one stream.
+ * Other arguments, validation and errors are those of attn_run_paged.
+ */
+attn_status_t attn_run_paged_no_workspace(attn_plan_t plan, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *page_table,
+                                          const int32_t *seq_lens, const int32_t *qo_indptr,
+                                          const float *sinks, int32_t window,
+                                          float softmax_scale, float k_scale, float v_scale,
+                                          void *out, float *lse_out, void *stream);
+
 /* Free a plan and its device memory (synchronises the plan's device).
  * NULL is accepted. */
 attn_status_t attn_plan_destroy(attn_plan_t plan);
