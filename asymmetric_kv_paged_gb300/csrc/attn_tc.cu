@@ -30,6 +30,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "kernels.hpp"
 #include "tc_common.cuh"
@@ -72,30 +73,49 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pv_done[2];
-  uint64_t o_free, final_done;
+  uint64_t o_free, final_done, sm_sync;
 };
 
-// Walks the CTA's tiles in order: segment, tile id, first/last flags.
+// Walks the CTA's tiles in order: segment, tile id, first/last flags.  The
+// current segment and its block are cached in registers, so a tile step reads
+// no memory unless it crosses into the next segment.
 struct Cursor {
   const SegDesc *segs;
+  const BlockDesc *blocks;
   int seg, seg_end, tile, si;
-  __device__ void init(const SegDesc *s, int b, int e) {
+  SegDesc sd;
+  BlockDesc bd;
+  __device__ void init(const SegDesc *s, const BlockDesc *b, int first, int end) {
     segs = s;
-    seg = b;
-    seg_end = e;
-    tile = s[b].tile_begin;
+    blocks = b;
+    seg = first;
+    seg_end = end;
     si = 0;
+    load();
   }
-  __device__ bool first() const { return tile == segs[seg].tile_begin; }
-  __device__ bool last() const { return tile + 1 == segs[seg].tile_end; }
+  __device__ void load() {
+    sd = segs[seg];
+    bd = blocks[sd.block];
+    tile = sd.tile_begin;
+  }
+  __device__ bool first() const { return tile == sd.tile_begin; }
+  __device__ bool last() const { return tile + 1 == sd.tile_end; }
   __device__ void next() {
-    if (++tile == segs[seg].tile_end && seg + 1 < seg_end) {
+    if (++tile == sd.tile_end && seg + 1 < seg_end) {
       ++seg;
       ++si;
-      tile = segs[seg].tile_begin;
+      load();
     }
   }
 };
+
+// Rows of a block are replicated across the 128 MMA rows when the block has
+// at most 64 rows: row position p holds block row p % rows_pad, so each copy
+// (p / rows_pad) of a row gets its own softmax thread, its own slice of every
+// key tile and its own O accumulator; copies are combined once per segment.
+__device__ __forceinline__ int rows_pad_of(int nrows) {
+  return nrows <= 8 ? 8 : nrows <= 16 ? 16 : nrows <= 32 ? 32 : nrows <= 64 ? 64 : 128;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -167,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ float sm_m[kRows], sm_l[kRows];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -194,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(&bars.o_free, 128);
     tc::mbar_init(&bars.final_done, 1);
+    tc::mbar_init(&bars.sm_sync, 128);
     tc::fence_mbar_init();
   }
   if (warp == 8) tc::tmem_alloc(&tmem_slot, kTmemCols);
@@ -211,12 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int oob = a.num_pages * a.page_size;              // first slot past the pool
       constexpr uint32_t kTileBytes = FP8 ? kRawBytes : kOpBytes;
       Cursor cur;
-      cur.init(a.segs, seg_begin, seg_end);
+      cur.init(a.segs, a.blocks, seg_begin, seg_end);
       for (int k = 0; k < total; ++k, cur.next()) {
         const int t = k % NT;
         uint64_t *empty = FP8 ? &bars.tma_empty[t] : &bars.op_empty[t];
         if (k >= NT && !tc::mbar_wait(empty, ((k / NT) - 1) & 1, &abort_flag)) break;
-        const BlockDesc bd = a.blocks[a.segs[cur.seg].block];
+        const BlockDesc &bd = cur.bd;
         const int32_t *pt_row = a.page_table + (int64_t)bd.b * a.pt_stride;
         const int key0 = cur.tile * kN;
         mbar_expect_tx(&bars.tma_full[t], kTileBytes);
@@ -253,14 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t *kc = static_cast<const uint8_t *>(a.k_cache);
     const uint8_t *vc = static_cast<const uint8_t *>(a.v_cache);
     Cursor cur;
-    cur.init(a.segs, seg_begin, seg_end);
+    cur.init(a.segs, a.blocks, seg_begin, seg_end);
     for (int k = 0; k < total; ++k, cur.next()) {
-      const SegDesc sd = a.segs[cur.seg];
-      const BlockDesc bd = a.blocks[sd.block];
+      const BlockDesc &bd = cur.bd;
       if (cur.first()) {
         if (cur.si > 0 && !tc::mbar_wait(&bars.q_empty, (cur.si - 1) & 1, &abort_flag)) break;
+        const int rows_pad = rows_pad_of(bd.nrows);
         for (int idx = ct; idx < kRows * 24; idx += 128) {
-          const int r = idx / 24;
+          const int p = idx / 24;          // MMA row position
+          const int r = p % rows_pad;      // block row it holds
           const int ch = idx % 24;
           uint4 v = make_uint4(0u, 0u, 0u, 0u);
           if (r < bd.nrows) {
@@ -271,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                       ((int64_t)tok * a.hq + h) * kDqk) + ch);
             if (kHalf) v = bf16x8_to_f16x8(v);
           }
-          *reinterpret_cast<uint4 *>(smem + (ch >> 3) * kQBlock + tc::sw128_offset(r, ch & 7)) = v;
+          *reinterpret_cast<uint4 *>(smem + (ch >> 3) * kQBlock + tc::sw128_offset(p, ch & 7)) = v;
         }
         tc::fence_proxy_async_smem();
         tc::mbar_arrive(&bars.q_full);
@@ -386,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_s = tc::idesc_f16(kHalf ? 0 : 1, 0, 0, kRows, kN);
       const uint32_t id_pv = tc::idesc_f16(kHalf ? 0 : 1, 0, 1, kRows, kDv);
       Cursor cs, cp;
-      cs.init(a.segs, seg_begin, seg_end);
-      cp.init(a.segs, seg_begin, seg_end);
+      cs.init(a.segs, a.blocks, seg_begin, seg_end);
+      cp.init(a.segs, a.blocks, seg_begin, seg_end);
       bool ok = true;
       auto issue_pv = [&](int k) -> bool {
         const int b = k & 1;
@@ -435,120 +458,189 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int r = tid;  // query row of the block == TMEM lane
+    const int t = tid;  // MMA row position == TMEM lane
+    const int lane = t & 31;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     Cursor cur;
-    cur.init(a.segs, seg_begin, seg_end);
+    cur.init(a.segs, a.blocks, seg_begin, seg_end);
     float m_run = -INFINITY, l_run = 0.f;
-    int row_lo = 0, row_hi = 0, tok = 0, h = 0;
+    int row_lo = 0, row_hi = 0, rr = 0, rows_pad = kRows, col0 = 0, off = 0, len = kN, nc = kN;
     bool valid = false, warp_live = false;
-    BlockDesc bd{};
+    uint32_t sync_phase = 0;
+    // bounded rendezvous of the 128 softmax threads
+    auto group_sync = [&]() -> bool {
+      tc::mbar_arrive(&bars.sm_sync);
+      const bool ok = tc::mbar_wait(&bars.sm_sync, sync_phase, &abort_flag);
+      sync_phase ^= 1;
+      return ok;
+    };
+    // one key tile: S slice from TMEM -> mask -> running max -> P slice to smem.
+    // NC key columns per thread (16, 32 or 64).  The 64-column case reads S
+    // from TMEM twice (max pass, then exp pass) to keep register use low.
+    auto tile_body = [&](auto nc_tag, int k) -> bool {
+      constexpr int NC = decltype(nc_tag)::value;
+      constexpr int NH = NC > 32 ? 32 : NC;     // columns held in registers at a time
+      const int b = k & 1;
+      const int key0 = cur.tile * kN + col0;
+      const bool whole = off == 0 && len == NC && key0 >= row_lo && key0 + NC <= row_hi;
+      auto load_scaled = [&](int q, float (&v)[NH]) {
+        uint32_t raw[NH];
+        if constexpr (NH == 16)
+          tc::tmem_ld16(tmem + lane_base + b * kN + col0, raw);
+        else
+          tc::tmem_ld32(tmem + lane_base + b * kN + col0 + 32 * q, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+          const int jj = q * NH + j;
+          const int key = key0 + jj;
+          const bool in = whole || (jj >= off && jj < off + len && key >= row_lo && key < row_hi);
+          v[j] = in ? __uint_as_float(raw[j]) * a.scale_log2 : -INFINITY;
+        }
+      };
+      if (!warp_live) {
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars.s_empty[b]);
+        if (k >= 2 && !tc::mbar_wait(&bars.pv_done[b], ((k - 2) >> 1) & 1, &abort_flag))
+          return false;
+        return true;
+      }
+      float v[NH];
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int q = 0; q < NC / NH; ++q) {
+        load_scaled(q, v);
+#pragma unroll
+        for (int j = 0; j < NH; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+      }
+      if constexpr (NC == NH) {      // values stay in registers: S may be reused now
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars.s_empty[b]);
+      }
+      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      if (cur.first()) {
+        m_run = m_tile;
+        l_run = 0.f;
+      } else {
+        const bool need = m_tile > m_run + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          if (!tc::mbar_wait(&bars.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, &abort_flag))
+            return false;
+          tc::tc_fence_after();
+          const float m_new = need ? m_tile : m_run;
+          const float alpha = need ? ex2(m_run - m_new) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < kDv / 32; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tc::tmem_st32(tmem + lane_base + kTmemO + c * 32, o);
+          }
+          tc::tmem_wait_st();
+          l_run *= alpha;
+          m_run = m_new;
+        }
+      }
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      if (k >= 2 && !tc::mbar_wait(&bars.pv_done[b], ((k - 2) >> 1) & 1, &abort_flag))
+        return false;
+      uint8_t *prow = smem + Lay::kOffP + b * kPBytes;
+      const int ch0 = col0 >> 3;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < NC / NH; ++q) {
+        if (NC != NH) load_scaled(q, v);
+        uint32_t pk[NH / 2];
+#pragma unroll
+        for (int j = 0; j < NH; j += 2) {
+          const float p0 = ex2(v[j] - m_use);
+          const float p1 = ex2(v[j + 1] - m_use);
+          rs[(j >> 1) & 3] += p0 + p1;
+          pk[j / 2] = cvt_pair(p0, p1, kHalf);
+        }
+#pragma unroll
+        for (int i = 0; i < NH / 8; ++i)
+          *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(t, ch0 + q * (NH / 8) + i)) =
+              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+      if constexpr (NC != NH) {      // second TMEM pass done: S may be reused now
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars.s_empty[b]);
+      }
+      l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      if constexpr (NC < kN) {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          if (ch < ch0 || ch >= ch0 + NC / 8)
+            *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(t, ch)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      tc::fence_proxy_async_smem();
+      return true;
+    };
+
     for (int k = 0; k < total; ++k, cur.next()) {
-      const SegDesc sd = a.segs[cur.seg];
-      const bool first = cur.first();
-      if (first) {
-        bd = a.blocks[sd.block];
-        valid = r < bd.nrows;
-        warp_live = warp * 32 < bd.nrows;
+      const BlockDesc &bd = cur.bd;
+      if (cur.first()) {
+        rows_pad = rows_pad_of(bd.nrows);
+        rr = t % rows_pad;
+        valid = rr < bd.nrows;
+        if (rows_pad <= 32) {          // 32 / rows_pad copies per warp, 16 key columns per warp
+          nc = 16;
+          col0 = 16 * warp;
+          len = rows_pad / 2;
+          off = (t / rows_pad) * len - col0;
+        } else if (rows_pad == 64) {   // two copies, 32 key columns each
+          nc = 32;
+          col0 = 32 * (warp >> 1);
+          len = 32;
+          off = 0;
+        } else {
+          nc = kN;
+          col0 = 0;
+          len = kN;
+          off = 0;
+        }
+        warp_live = __any_sync(0xffffffffu, valid);
         row_lo = row_hi = 0;
         if (valid) {
-          const int flat = bd.row0 + r;
-          const int t = flat / a.group;
-          tok = bd.tok0 + t;
-          h = bd.g * a.group + flat % a.group;
-          const int i = bd.L - bd.n + t;
+          const int i = bd.L - bd.n + (bd.row0 + rr) / a.group;
           row_hi = i + 1;
           row_lo = a.window > 0 ? max(0, i - a.window + 1) : 0;
         }
+        m_run = -INFINITY;
+        l_run = 0.f;
       }
       const int b = k & 1;
       if (!tc::mbar_wait(&bars.s_full[b], (k >> 1) & 1, &abort_flag)) break;
       tc::tc_fence_after();
-      float sv[kN];
-      if (warp_live) {
-        uint32_t raw[32];
-        tc::tmem_ld32(tmem + lane_base + b * kN, raw);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
-        tc::tmem_ld32(tmem + lane_base + b * kN + 32, raw);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(raw[j]);
-      }
-      tc::tc_fence_before();
-      tc::mbar_arrive(&bars.s_empty[b]);
-
-      if (warp_live) {
-        const int key0 = cur.tile * kN;
-        float m_tile = -INFINITY;
-        if (key0 >= row_lo && key0 + kN <= row_hi) {
-#pragma unroll
-          for (int j = 0; j < kN; ++j) {
-            sv[j] *= a.scale_log2;
-            m_tile = fmaxf(m_tile, sv[j]);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < kN; ++j) {
-            const int key = key0 + j;
-            sv[j] = (key >= row_lo && key < row_hi) ? sv[j] * a.scale_log2 : -INFINITY;
-            m_tile = fmaxf(m_tile, sv[j]);
-          }
-        }
-        if (first) {
-          m_run = m_tile;
-          l_run = 0.f;
-        } else {
-          const bool need = m_tile > m_run + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            if (!tc::mbar_wait(&bars.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, &abort_flag)) break;
-            tc::tc_fence_after();
-            const float m_new = need ? m_tile : m_run;
-            const float alpha = need ? ex2(m_run - m_new) : 1.f;
-#pragma unroll
-            for (int c = 0; c < kDv / 32; ++c) {
-              uint32_t o[32];
-              tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
-              tc::tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-              tc::tmem_st32(tmem + lane_base + kTmemO + c * 32, o);
-            }
-            tc::tmem_wait_st();
-            l_run *= alpha;
-            m_run = m_new;
-          }
-        }
-        const float m_use = m_run == -INFINITY ? 0.f : m_run;
-        uint32_t pk[kN / 2];
-        float rs = 0.f;
-#pragma unroll
-        for (int j = 0; j < kN; j += 2) {
-          const float p0 = ex2(sv[j] - m_use);
-          const float p1 = ex2(sv[j + 1] - m_use);
-          rs += p0 + p1;
-          pk[j / 2] = cvt_pair(p0, p1, kHalf);
-        }
-        l_run += rs;
-        if (k >= 2 && !tc::mbar_wait(&bars.pv_done[b], ((k - 2) >> 1) & 1, &abort_flag)) break;
-        uint8_t *pb = smem + Lay::kOffP + b * kPBytes;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4 *>(pb + tc::sw128_offset(r, c)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        tc::fence_proxy_async_smem();
-      } else if (k >= 2 && !tc::mbar_wait(&bars.pv_done[b], ((k - 2) >> 1) & 1, &abort_flag)) {
-        break;
-      }
+      bool ok;
+      if (nc == 16)
+        ok = tile_body(std::integral_constant<int, 16>{}, k);
+      else if (nc == 32)
+        ok = tile_body(std::integral_constant<int, 32>{}, k);
+      else
+        ok = tile_body(std::integral_constant<int, 64>{}, k);
+      if (!ok) break;
       tc::tc_fence_before();
       tc::mbar_arrive(&bars.p_full[b]);
+      if (!cur.last()) continue;
 
-      if (cur.last()) {
-        if (!tc::mbar_wait(&bars.pv_done[b], (k >> 1) & 1, &abort_flag)) break;
-        tc::tc_fence_after();
+      // ---------------- end of segment: normalise and write the block's rows
+      if (!tc::mbar_wait(&bars.pv_done[b], (k >> 1) & 1, &abort_flag)) break;
+      tc::tc_fence_after();
+      const SegDesc &sd = cur.sd;
+      const bool single = bd.num_splits == 1;
+      if (rows_pad == kRows) {
+        // one copy per row: thread t owns row t outright
         if (warp_live) {
-          const bool single = bd.num_splits == 1;
+          int tok = 0, h = 0;
+          if (valid) {
+            const int flat = bd.row0 + t;
+            tok = bd.tok0 + flat / a.group;
+            h = bd.g * a.group + flat % a.group;
+          }
           float scale_o = 0.f, lse = -INFINITY;
           if (single) {
             const float sig = (a.sinks && valid) ? a.sinks[h] * kLog2e : -INFINITY;
@@ -562,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             scale_o = l_run > 0.f ? a.v_scale / l_run : 0.f;
             lse = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
           }
-          const int prow = bd.part_row_base + sd.split * bd.nrows + r;
+          const int prow = bd.part_row_base + sd.split * bd.nrows + t;
 #pragma unroll
           for (int c = 0; c < kDv / 32; ++c) {
             uint32_t o[32];
@@ -599,9 +691,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tc::tc_fence_before();
-        tc::mbar_arrive(&bars.o_free);
+      } else {
+        // several copies per row: combine them through shared memory.
+        // sm_m / sm_l: each copy's running max and sum; buf: 32 O columns per
+        // copy at a time, scaled to the row's common max (stride 33: no bank
+        // conflicts); each thread then sums the copies of (row, column) pairs.
+        const int copies = kRows / rows_pad;
+        sm_m[t] = valid ? m_run : -INFINITY;
+        sm_l[t] = valid ? l_run : 0.f;
+        if (!group_sync()) break;
+        float f = 0.f;
+        if (valid && m_run != -INFINITY) {
+          float M = -INFINITY;
+          for (int c = 0; c < copies; ++c) M = fmaxf(M, sm_m[c * rows_pad + rr]);
+          f = exp2f(m_run - M);
+        }
+        float *buf = reinterpret_cast<float *>(smem + Lay::kOffP);
+        const int nout = rows_pad / 4;   // (row, column) outputs per thread per chunk
+        bool sync_ok = true;
+#pragma unroll 1
+        for (int c = 0; c < kDv / 32; ++c) {
+          if (warp_live) {
+            uint32_t o[32];
+            tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) buf[t * 33 + j] = valid ? f * __uint_as_float(o[j]) : 0.f;
+          }
+          sync_ok = group_sync() && sync_ok;
+#pragma unroll 1
+          for (int i = 0; i < nout; ++i) {
+            const int row = (t >> 5) + 4 * i;
+            if (!sync_ok || row >= bd.nrows) continue;
+            float v = 0.f, M = -INFINITY, L = 0.f;
+            for (int cp2 = 0; cp2 < copies; ++cp2) {
+              v += buf[(cp2 * rows_pad + row) * 33 + lane];
+              M = fmaxf(M, sm_m[cp2 * rows_pad + row]);
+            }
+            if (M != -INFINITY)
+              for (int cp2 = 0; cp2 < copies; ++cp2) {
+                const float mc = sm_m[cp2 * rows_pad + row];
+                if (mc != -INFINITY) L += sm_l[cp2 * rows_pad + row] * exp2f(mc - M);
+              }
+            const int flat = bd.row0 + row;
+            const int tok = bd.tok0 + flat / a.group;
+            const int h = bd.g * a.group + flat % a.group;
+            if (single) {
+              const float sig = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
+              const float MM = fmaxf(M, sig);
+              float scale_o = 0.f, lse = -INFINITY;
+              if (MM != -INFINITY) {
+                const float Z = L * exp2f(M - MM) + exp2f(sig - MM);
+                scale_o = exp2f(M - MM) * a.v_scale / Z;
+                lse = (MM + log2f(Z)) * kLn2;
+              }
+              static_cast<__nv_bfloat16 *>(a.out)[((int64_t)tok * a.hq + h) * kDv + 32 * c + lane] =
+                  __float2bfloat16_rn(v * scale_o);
+              if (c == 0 && lane == 0 && a.lse_out) a.lse_out[(int64_t)tok * a.hq + h] = lse;
+            } else {
+              const int prow = bd.part_row_base + sd.split * bd.nrows + row;
+              a.part_o[(int64_t)prow * kDv + 32 * c + lane] = L > 0.f ? v * a.v_scale / L : 0.f;
+              if (c == 0 && lane == 0) a.part_lse[prow] = L > 0.f ? M + log2f(L) : -INFINITY;
+            }
+          }
+          sync_ok = group_sync() && sync_ok;
+        }
+        if (!sync_ok) break;
       }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars.o_free);
     }
   }
 
