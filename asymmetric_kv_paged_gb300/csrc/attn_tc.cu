@@ -177,7 +177,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 
 template <bool FP8, bool TMA>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const RunArgs a, const __grid_constant__ TmaMaps maps) {
+    attn_tc_kernel(const RunArgs args, const __grid_constant__ TmaMaps maps) {
+  // A plain local copy of the arguments: the role lambdas capture by reference,
+  // and a reference into kernel-parameter space would turn every field read
+  // inside them into a memory load that the K/V stream keeps evicting.
+  const RunArgs a = args;
   using Lay = Layout<FP8>;
   constexpr int NS = Lay::kOpStages;
   constexpr int NT = Lay::kTmaStages;

@@ -86,10 +86,10 @@ def peaks():
 
 
 def split_kernel_traffic(workload: str):
-    """DRAM bytes per launch of the split-KV kernel from a committed ncu summary,
+    """DRAM bytes per launch of the attention kernel from a committed ncu summary,
     when that summary was taken on the kernel source as it is now (else None)."""
-    path = os.path.join(ROOT, "profiles", f"split_kv_{workload}.md")
-    src = os.path.join(ROOT, "asymmetric_kv_paged_gb300", "csrc", "split_kv.cu")
+    path = os.path.join(ROOT, "profiles", f"attn_tc_{workload}.md")
+    src = os.path.join(ROOT, "asymmetric_kv_paged_gb300", "csrc", "attn_tc.cu")
     if not os.path.exists(path):
         return None
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -381,7 +381,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world} (independent requests, no collective)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": split_kernel_traffic(args.workload),
-                     "kernel": "split_kv_kernel", "kernel_ms": split_ms, "merge_ms": r["merge_ms"],
+                     "kernel": "attn_tc_kernel", "kernel_ms": split_ms, "merge_ms": r["merge_ms"],
                      "peak_source": f"{pk['source']} (hbm_gbs)"},
         "e2e": {"value": nbytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
