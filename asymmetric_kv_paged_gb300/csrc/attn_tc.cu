@@ -96,8 +96,16 @@ struct Cursor {
   __device__ void load() {
     sd = segs[seg];
     bd = blocks[sd.block];
+    // Pin every field in a register: without this the compiler may re-read a
+    // field from global memory at each later use (it may assume the kernel's
+    // float / bf16 stores cannot alias these ints), and under the K/V stream
+    // such a re-read costs a DRAM round trip on every tile.
+    pin(sd.block); pin(sd.tile_begin); pin(sd.tile_end); pin(sd.split);
+    pin(bd.b); pin(bd.g); pin(bd.row0); pin(bd.nrows); pin(bd.L); pin(bd.n);
+    pin(bd.tok0); pin(bd.klo); pin(bd.khi); pin(bd.num_splits); pin(bd.part_row_base);
     tile = sd.tile_begin;
   }
+  static __device__ __forceinline__ void pin(int32_t &x) { asm volatile("" : "+r"(x)); }
   __device__ bool first() const { return tile == sd.tile_begin; }
   __device__ bool last() const { return tile + 1 == sd.tile_end; }
   __device__ void next() {
@@ -240,34 +248,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       cur.init(a.segs, a.blocks, seg_begin, seg_end);
       for (int k = 0; k < total; ++k, cur.next()) {
         const int t = k % NT;
-        uint64_t *empty = FP8 ? &bars.tma_empty[t] : &bars.op_empty[t];
-        if (k >= NT && !tc::mbar_wait(empty, ((k / NT) - 1) & 1, &abort_flag)) break;
         const BlockDesc &bd = cur.bd;
         const int32_t *pt_row = a.page_table + (int64_t)bd.b * a.pt_stride;
         const int key0 = cur.tile * kN;
-        mbar_expect_tx(&bars.tma_full[t], kTileBytes);
-        const uint32_t dst = sbase + (FP8 ? Lay::kOffRaw + t * kRawBytes : Lay::kOffOp + t * kOpBytes);
-        for (int i = 0; i < nbox; ++i) {
+        // page-table lookups first: their latency overlaps the wait for a free stage
+        int slot[kN / 8];
+#pragma unroll
+        for (int i = 0; i < kN / 8; ++i) {
+          slot[i] = oob;  // boxes with no visible key read past the pool: zero fill
           const int j = key0 + i * box;
-          int slot = oob;  // boxes with no visible key read past the pool: zero fill
-          if (j + box > bd.klo && j < bd.khi) {
+          if (i < nbox && j + box > bd.klo && j < bd.khi) {
             const int32_t page = __ldg(pt_row + j / a.page_size);
             if (page >= 0 && page < a.num_pages)
-              slot = page * a.page_size + j % a.page_size;
+              slot[i] = page * a.page_size + j % a.page_size;
             else
               atomicOr(a.err, 1);
           }
+        }
+        uint64_t *empty = FP8 ? &bars.tma_empty[t] : &bars.op_empty[t];
+        if (k >= NT && !tc::mbar_wait(empty, ((k / NT) - 1) & 1, &abort_flag)) break;
+        mbar_expect_tx(&bars.tma_full[t], kTileBytes);
+        const uint32_t dst = sbase + (FP8 ? Lay::kOffRaw + t * kRawBytes : Lay::kOffOp + t * kOpBytes);
+#pragma unroll
+        for (int i = 0; i < kN / 8; ++i) {
+          if (i >= nbox) break;
           if (FP8) {
-            tma_load_3d(dst + i * box * kDqk, &maps.k, 0, bd.g, slot, &bars.tma_full[t]);
-            tma_load_3d(dst + kRawK + i * box * kDv, &maps.v, 0, bd.g, slot, &bars.tma_full[t]);
+            tma_load_3d(dst + i * box * kDqk, &maps.k, 0, bd.g, slot[i], &bars.tma_full[t]);
+            tma_load_3d(dst + kRawK + i * box * kDv, &maps.v, 0, bd.g, slot[i], &bars.tma_full[t]);
           } else {
 #pragma unroll
             for (int c = 0; c < 3; ++c)
-              tma_load_3d(dst + c * kBlk + i * box * 128, &maps.k, 64 * c, bd.g, slot,
+              tma_load_3d(dst + c * kBlk + i * box * 128, &maps.k, 64 * c, bd.g, slot[i],
                           &bars.tma_full[t]);
 #pragma unroll
             for (int c = 0; c < 2; ++c)
-              tma_load_3d(dst + kOpK + c * kBlk + i * box * 128, &maps.v, 64 * c, bd.g, slot,
+              tma_load_3d(dst + kOpK + c * kBlk + i * box * 128, &maps.v, 64 * c, bd.g, slot[i],
                           &bars.tma_full[t]);
           }
         }
@@ -412,51 +427,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((tid & 31) == 0) {
       const uint32_t id_s = tc::idesc_f16(kHalf ? 0 : 1, 0, 0, kRows, kN);
       const uint32_t id_pv = tc::idesc_f16(kHalf ? 0 : 1, 0, 1, kRows, kDv);
+      // Two streams of work, S = Q.K^T per tile and O += P.V per tile, issued in
+      // tile order each but interleaved by readiness: P.V of tile k goes out as
+      // soon as its P is written, without waiting for tile k+1's K to land.
       Cursor cs, cp;
       cs.init(a.segs, a.blocks, seg_begin, seg_end);
       cp.init(a.segs, a.blocks, seg_begin, seg_end);
-      bool ok = true;
-      auto issue_pv = [&](int k) -> bool {
-        const int b = k & 1;
-        const int s = k % NS;
-        if (!tc::mbar_wait(&bars.p_full[b], (k >> 1) & 1, &abort_flag)) return false;
-        const bool first = cp.first();
-        if (first && cp.si > 0 && !tc::mbar_wait(&bars.o_free, (cp.si - 1) & 1, &abort_flag))
-          return false;
-        tc::tc_fence_after();
-        const uint32_t pb = sbase + Lay::kOffP + b * kPBytes;
-        const uint32_t vb = sbase + Lay::kOffOp + s * kOpBytes + kOpK;
+      int ks = 0, kp = 0;
+      uint64_t idle_since = 0;
+      constexpr uint32_t kPoll = 64;   // ns of hardware sleep per barrier probe
+      while (kp < total) {
+        bool progressed = false;
+        if (ks < total) {
+          const int s = ks % NS;
+          const int b = ks & 1;
+          const bool ready =
+              (!cs.first() || tc::mbar_try_wait(tc::smem_u32(&bars.q_full), cs.si & 1, kPoll)) &&
+              tc::mbar_try_wait(tc::smem_u32(&bars.op_full[s]), (ks / NS) & 1, kPoll) &&
+              (ks < 2 ||
+               tc::mbar_try_wait(tc::smem_u32(&bars.s_empty[b]), ((ks >> 1) - 1) & 1, kPoll));
+          if (ready) {
+            tc::tc_fence_after();
+            const uint32_t kb = sbase + Lay::kOffOp + s * kOpBytes;
 #pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk) {
-          const uint64_t ad = tc::smem_desc_sw128(pb + kk * 32, 16, 1024);
-          const uint64_t bdsc = tc::smem_desc_sw128(vb + kk * 16 * 128, kBlk, 1024);
-          tc::mma_f16_ss(tmem + kTmemO, ad, bdsc, id_pv, (!first || kk > 0) ? 1u : 0u);
+            for (int kq = 0; kq < kDqk / 16; ++kq) {
+              const uint32_t koff = (kq & 3) * 32;
+              const uint64_t ad = tc::smem_desc_sw128(sbase + (kq >> 2) * kQBlock + koff, 16, 1024);
+              const uint64_t bdsc = tc::smem_desc_sw128(kb + (kq >> 2) * kBlk + koff, 16, 1024);
+              tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, kq > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(&bars.s_full[b]);
+            if (cs.last()) tc::mma_commit(&bars.q_empty);
+            cs.next();
+            ++ks;
+            progressed = true;
+          }
         }
-        tc::mma_commit(&bars.op_empty[s]);
-        tc::mma_commit(&bars.pv_done[b]);
-        cp.next();
-        return true;
-      };
-      for (int k = 0; k < total && ok; ++k, cs.next()) {
-        const int s = k % NS;
-        const int b = k & 1;
-        if (cs.first() && !tc::mbar_wait(&bars.q_full, cs.si & 1, &abort_flag)) break;
-        if (!tc::mbar_wait(&bars.op_full[s], (k / NS) & 1, &abort_flag)) break;
-        if (k >= 2 && !tc::mbar_wait(&bars.s_empty[b], ((k >> 1) - 1) & 1, &abort_flag)) break;
-        tc::tc_fence_after();
-        const uint32_t kb = sbase + Lay::kOffOp + s * kOpBytes;
+        if (kp < ks) {
+          const int b = kp & 1;
+          const int s = kp % NS;
+          const bool first = cp.first();
+          const bool ready =
+              tc::mbar_try_wait(tc::smem_u32(&bars.p_full[b]), (kp >> 1) & 1, kPoll) &&
+              (!first || cp.si == 0 ||
+               tc::mbar_try_wait(tc::smem_u32(&bars.o_free), (cp.si - 1) & 1, kPoll));
+          if (ready) {
+            tc::tc_fence_after();
+            const uint32_t pb = sbase + Lay::kOffP + b * kPBytes;
+            const uint32_t vb = sbase + Lay::kOffOp + s * kOpBytes + kOpK;
 #pragma unroll
-        for (int ks = 0; ks < kDqk / 16; ++ks) {
-          const uint32_t koff = (ks & 3) * 32;
-          const uint64_t ad = tc::smem_desc_sw128(sbase + (ks >> 2) * kQBlock + koff, 16, 1024);
-          const uint64_t bdsc = tc::smem_desc_sw128(kb + (ks >> 2) * kBlk + koff, 16, 1024);
-          tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, ks > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kN / 16; ++kk) {
+              const uint64_t ad = tc::smem_desc_sw128(pb + kk * 32, 16, 1024);
+              const uint64_t bdsc = tc::smem_desc_sw128(vb + kk * 16 * 128, kBlk, 1024);
+              tc::mma_f16_ss(tmem + kTmemO, ad, bdsc, id_pv, (!first || kk > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(&bars.op_empty[s]);
+            tc::mma_commit(&bars.pv_done[b]);
+            cp.next();
+            ++kp;
+            progressed = true;
+          }
         }
-        tc::mma_commit(&bars.s_full[b]);
-        if (cs.last()) tc::mma_commit(&bars.q_empty);
-        if (k >= 1) ok = issue_pv(k - 1);
+        if (progressed) {
+          idle_since = 0;
+        } else {
+          // bounded like every other wait: give up after 2 s without progress
+          if (abort_flag) break;
+          const uint64_t now = tc::globaltimer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (now - idle_since > 2000000000ull) {
+            abort_flag = 1;
+            break;
+          }
+        }
       }
-      if (ok && !abort_flag) issue_pv(total - 1);
       tc::mma_commit(&bars.final_done);
       tc::mbar_wait(&bars.final_done, 0, &abort_flag);
     }
@@ -485,8 +530,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int NC = decltype(nc_tag)::value;
       constexpr int NH = NC > 32 ? 32 : NC;     // columns held in registers at a time
       const int b = k & 1;
+      // visible columns of this thread in the warp's NC-column window: its own
+      // slice [off, off + len) clipped to the row's keys [row_lo, row_hi)
       const int key0 = cur.tile * kN + col0;
-      const bool whole = off == 0 && len == NC && key0 >= row_lo && key0 + NC <= row_hi;
+      const int j_lo = max(off, row_lo - key0);
+      const int j_hi = min(off + len, row_hi - key0);
       auto load_scaled = [&](int q, float (&v)[NH]) {
         uint32_t raw[NH];
         if constexpr (NH == 16)
@@ -497,8 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
           const int jj = q * NH + j;
-          const int key = key0 + jj;
-          const bool in = whole || (jj >= off && jj < off + len && key >= row_lo && key < row_hi);
+          const bool in = (jj >= j_lo) & (jj < j_hi);
           v[j] = in ? __uint_as_float(raw[j]) * a.scale_log2 : -INFINITY;
         }
       };
