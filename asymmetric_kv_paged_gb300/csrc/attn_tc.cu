@@ -68,7 +68,7 @@ struct Layout {
 };
 
 struct Bars {
-  uint64_t tma_full[3], tma_empty[3];
+  uint64_t tma_full[3], tma_empty[3], edge_full[3];
   uint64_t op_full[3], op_empty[3];
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];
@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 3; ++s) {
       tc::mbar_init(&bars.tma_full[s], 1);
       tc::mbar_init(&bars.tma_empty[s], 128);
+      tc::mbar_init(&bars.edge_full[s], 1);
       tc::mbar_init(&bars.op_full[s], 128);
       tc::mbar_init(&bars.op_empty[s], 1);
     }
@@ -267,23 +268,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint64_t *empty = FP8 ? &bars.tma_empty[t] : &bars.op_empty[t];
         if (k >= NT && !tc::mbar_wait(empty, ((k / NT) - 1) & 1, &abort_flag)) break;
-        mbar_expect_tx(&bars.tma_full[t], kTileBytes);
+        // BF16: a tile with keys outside the block's range lands on edge_full, which
+        // only the converters wait on (they zero those V rows); every other tile
+        // lands on tma_full, which only the MMA warp waits on.
+        const bool edge = !FP8 && (key0 < bd.klo || key0 + kN > bd.khi);
+        uint64_t *full = edge ? &bars.edge_full[t] : &bars.tma_full[t];
+        mbar_expect_tx(full, kTileBytes);
         const uint32_t dst = sbase + (FP8 ? Lay::kOffRaw + t * kRawBytes : Lay::kOffOp + t * kOpBytes);
 #pragma unroll
         for (int i = 0; i < kN / 8; ++i) {
           if (i >= nbox) break;
           if (FP8) {
-            tma_load_3d(dst + i * box * kDqk, &maps.k, 0, bd.g, slot[i], &bars.tma_full[t]);
-            tma_load_3d(dst + kRawK + i * box * kDv, &maps.v, 0, bd.g, slot[i], &bars.tma_full[t]);
+            tma_load_3d(dst + i * box * kDqk, &maps.k, 0, bd.g, slot[i], full);
+            tma_load_3d(dst + kRawK + i * box * kDv, &maps.v, 0, bd.g, slot[i], full);
           } else {
 #pragma unroll
             for (int c = 0; c < 3; ++c)
               tma_load_3d(dst + c * kBlk + i * box * 128, &maps.k, 64 * c, bd.g, slot[i],
-                          &bars.tma_full[t]);
+                          full);
 #pragma unroll
             for (int c = 0; c < 2; ++c)
               tma_load_3d(dst + kOpK + c * kBlk + i * box * 128, &maps.v, 64 * c, bd.g, slot[i],
-                          &bars.tma_full[t]);
+                          full);
           }
         }
       }
@@ -295,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t *vc = static_cast<const uint8_t *>(a.v_cache);
     Cursor cur;
     cur.init(a.segs, a.blocks, seg_begin, seg_end);
+    uint32_t edge_parity = 0;   // BF16 + TMA: completed edge tiles per stage (one bit each)
     for (int k = 0; k < total; ++k, cur.next()) {
       const BlockDesc &bd = cur.bd;
       if (cur.first()) {
@@ -322,9 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key0 = cur.tile * kN;
       uint8_t *op = smem + Lay::kOffOp + s * kOpBytes;
       if (TMA && !FP8) {
-        // BF16 tile landed by TMA in operand layout; zero V rows outside the range
-        if (!tc::mbar_wait(&bars.tma_full[s], (k / NS) & 1, &abort_flag)) break;
-        if (key0 < bd.klo || key0 + kN > bd.khi) {
+        // BF16 tile landed by TMA in operand layout.  Interior tiles go straight
+        // to the MMA warp; on edge tiles zero the V rows outside the range first.
+        if (key0 >= bd.klo && key0 + kN <= bd.khi) continue;
+        if (!tc::mbar_wait(&bars.edge_full[s], (edge_parity >> s) & 1, &abort_flag)) break;
+        edge_parity ^= 1u << s;
+        {
           for (int idx = ct; idx < kN * 16; idx += 128) {
             const int kk = idx >> 4;
             const int j = key0 + kk;
@@ -435,34 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp.init(a.segs, a.blocks, seg_begin, seg_end);
       int ks = 0, kp = 0;
       uint64_t idle_since = 0;
+      // BF16 + TMA: interior tiles are consumed straight off the TMA barrier;
+      // edge tiles wait for the converters, whose barrier then completes only
+      // on edge tiles (one parity bit per stage).
+      uint32_t edge_parity = 0, inner_parity = 0;
       constexpr uint32_t kPoll = 64;   // ns of hardware sleep per barrier probe
       while (kp < total) {
         bool progressed = false;
-        if (ks < total) {
-          const int s = ks % NS;
-          const int b = ks & 1;
-          const bool ready =
-              (!cs.first() || tc::mbar_try_wait(tc::smem_u32(&bars.q_full), cs.si & 1, kPoll)) &&
-              tc::mbar_try_wait(tc::smem_u32(&bars.op_full[s]), (ks / NS) & 1, kPoll) &&
-              (ks < 2 ||
-               tc::mbar_try_wait(tc::smem_u32(&bars.s_empty[b]), ((ks >> 1) - 1) & 1, kPoll));
-          if (ready) {
-            tc::tc_fence_after();
-            const uint32_t kb = sbase + Lay::kOffOp + s * kOpBytes;
-#pragma unroll
-            for (int kq = 0; kq < kDqk / 16; ++kq) {
-              const uint32_t koff = (kq & 3) * 32;
-              const uint64_t ad = tc::smem_desc_sw128(sbase + (kq >> 2) * kQBlock + koff, 16, 1024);
-              const uint64_t bdsc = tc::smem_desc_sw128(kb + (kq >> 2) * kBlk + koff, 16, 1024);
-              tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, kq > 0 ? 1u : 0u);
-            }
-            tc::mma_commit(&bars.s_full[b]);
-            if (cs.last()) tc::mma_commit(&bars.q_empty);
-            cs.next();
-            ++ks;
-            progressed = true;
-          }
-        }
         if (kp < ks) {
           const int b = kp & 1;
           const int s = kp % NS;
@@ -485,6 +474,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit(&bars.pv_done[b]);
             cp.next();
             ++kp;
+            progressed = true;
+          }
+        }
+        if (ks < total) {
+          const int s = ks % NS;
+          const int b = ks & 1;
+          const int key0 = cs.tile * kN;
+          const bool edge = !(TMA && !FP8) || key0 < cs.bd.klo || key0 + kN > cs.bd.khi;
+          const bool land = edge ? tc::mbar_try_wait(tc::smem_u32(&bars.op_full[s]),
+                                                     (TMA && !FP8) ? (edge_parity >> s) & 1
+                                                                   : (ks / NS) & 1,
+                                                     kPoll)
+                                 : tc::mbar_try_wait(tc::smem_u32(&bars.tma_full[s]),
+                                                     (inner_parity >> s) & 1, kPoll);
+          const bool ready =
+              (!cs.first() || tc::mbar_try_wait(tc::smem_u32(&bars.q_full), cs.si & 1, kPoll)) &&
+              land &&
+              (ks < 2 ||
+               tc::mbar_try_wait(tc::smem_u32(&bars.s_empty[b]), ((ks >> 1) - 1) & 1, kPoll));
+          if (ready) {
+            if (TMA && !FP8) {
+              if (edge)
+                edge_parity ^= 1u << s;
+              else
+                inner_parity ^= 1u << s;
+            }
+            tc::tc_fence_after();
+            const uint32_t kb = sbase + Lay::kOffOp + s * kOpBytes;
+#pragma unroll
+            for (int kq = 0; kq < kDqk / 16; ++kq) {
+              const uint32_t koff = (kq & 3) * 32;
+              const uint64_t ad = tc::smem_desc_sw128(sbase + (kq >> 2) * kQBlock + koff, 16, 1024);
+              const uint64_t bdsc = tc::smem_desc_sw128(kb + (kq >> 2) * kBlk + koff, 16, 1024);
+              tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, kq > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(&bars.s_full[b]);
+            if (cs.last()) tc::mma_commit(&bars.q_empty);
+            cs.next();
+            ++ks;
             progressed = true;
           }
         }
