@@ -281,7 +281,7 @@ attn_status_t attn_plan_info(attn_plan_t plan, int32_t info[8]) {
   info[0] = (int32_t)hp.blocks.size();
   info[1] = (int32_t)hp.segs.size();
   info[2] = hp.num_ctas;
-  info[3] = akp::kBlockRows;
+  info[3] = hp.block_rows;
   info[4] = akp::kKeyTile;
   info[5] = hp.multi_split_blocks;
   info[6] = (int32_t)(hp.workspace_bytes & 0x7FFFFFFF);

@@ -38,26 +38,28 @@
 namespace akp {
 namespace {
 
-constexpr int kRows = 128;
 constexpr int kN = kKeyTile;                 // keys per tile (64)
 constexpr int kThreads = 10 * 32;
 constexpr int kBlk = kN * 128;               // one 64-column block of a 64-row tile: 8 KB
-constexpr int kQBlock = kRows * 128;         // one 64-column block of Q: 16 KB
-constexpr int kQBytes = 3 * kQBlock;         // 48 KB
 constexpr int kOpK = 3 * kBlk;               // K operand tile: 24 KB
 constexpr int kOpBytes = kOpK + 2 * kBlk;    // + V operand tile: 40 KB
 constexpr int kRawK = kN * kDqk;             // raw E4M3 K rows: 12 KB
 constexpr int kRawBytes = kRawK + kN * kDv;  // + raw V rows: 20 KB
-constexpr int kPBytes = kRows * 128;         // P tile [128 rows x 64 keys]: 16 KB
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemO = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;    // base-2 growth allowed before O is rescaled
 
-template <bool FP8>
+// Shared-memory layout for MR MMA rows (64 or 128): Q as three 64-column
+// blocks of MR rows, the K/V operand ring, the FP8 staging ring, and two P
+// tiles.  The smaller Q and P of MR = 64 leave room for one more K/V stage.
+template <bool FP8, int MR>
 struct Layout {
-  static constexpr int kOpStages = FP8 ? 2 : 3;
+  static constexpr int kQBlock = MR * 128;    // one 64-column block of Q
+  static constexpr int kQBytes = 3 * kQBlock;
+  static constexpr int kPBytes = MR * 128;    // P tile [MR rows x 64 keys]
+  static constexpr int kOpStages = FP8 ? (MR == 64 ? 3 : 2) : (MR == 64 ? 4 : 3);
   static constexpr int kRawStages = FP8 ? 3 : 0;
   static constexpr int kOffOp = kQBytes;
   static constexpr int kOffRaw = kOffOp + kOpStages * kOpBytes;
@@ -65,11 +67,13 @@ struct Layout {
   static constexpr int kUsed = kOffP + 2 * kPBytes;
   static constexpr int kSmem = kUsed + 1024;  // room to align the base to 1024 B
   static constexpr int kTmaStages = FP8 ? kRawStages : kOpStages;
+  // 227 KB per CTA, less the 2 KB of static shared memory.
+  static_assert(kSmem + 2048 <= 227 * 1024, "shared memory layout too large");
 };
 
 struct Bars {
-  uint64_t tma_full[3], tma_empty[3], edge_full[3];
-  uint64_t op_full[3], op_empty[3];
+  uint64_t tma_full[4], tma_empty[4], edge_full[4];
+  uint64_t op_full[4], op_empty[4];
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pv_done[2];
@@ -183,14 +187,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-template <bool FP8, bool TMA>
+template <bool FP8, bool TMA, int MR>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const RunArgs args, const __grid_constant__ TmaMaps maps) {
   // A plain local copy of the arguments: the role lambdas capture by reference,
   // and a reference into kernel-parameter space would turn every field read
   // inside them into a memory load that the K/V stream keeps evicting.
   const RunArgs a = args;
-  using Lay = Layout<FP8>;
+  using Lay = Layout<FP8, MR>;
+  constexpr int kRows = MR;                 // MMA rows (M)
+  constexpr int kQBlock = Lay::kQBlock;
+  constexpr int kPBytes = Lay::kPBytes;
   constexpr int NS = Lay::kOpStages;
   constexpr int NT = Lay::kTmaStages;
   constexpr bool kHalf = FP8;  // operand type: fp16 for FP8 caches, bf16 otherwise
@@ -199,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ float sm_m[kRows], sm_l[kRows];
+  __shared__ float sm_m[128], sm_l[128];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     abort_flag = 0;
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < 4; ++s) {
       tc::mbar_init(&bars.tma_full[s], 1);
       tc::mbar_init(&bars.tma_empty[s], 128);
       tc::mbar_init(&bars.edge_full[s], 1);
@@ -535,8 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int t = tid;  // MMA row position == TMEM lane
+    const int t = tid;
     const int lane = t & 31;
+    // MMA row position held in this thread's TMEM lane: with M = 128 row p is
+    // lane p; with M = 64 rows 16w..16w+15 sit in lanes 0-15 of warp w's
+    // subpartition and lanes 16-31 hold no row (pos = -1).
+    const int pos = kRows == 128 ? t : (lane < 16 ? warp * 16 + lane : -1);
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     Cursor cur;
     cur.init(a.segs, a.blocks, seg_begin, seg_end);
@@ -641,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < NH / 8; ++i)
-          *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(t, ch0 + q * (NH / 8) + i)) =
+          if (pos >= 0)
+            *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch0 + q * (NH / 8) + i)) =
               make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
       if constexpr (NC != NH) {      // second TMEM pass done: S may be reused now
@@ -652,8 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (NC < kN) {
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
-          if (ch < ch0 || ch >= ch0 + NC / 8)
-            *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(t, ch)) = make_uint4(0u, 0u, 0u, 0u);
+          if (pos >= 0 && (ch < ch0 || ch >= ch0 + NC / 8))
+            *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch)) = make_uint4(0u, 0u, 0u, 0u);
       }
       tc::fence_proxy_async_smem();
       return true;
@@ -663,22 +675,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const BlockDesc &bd = cur.bd;
       if (cur.first()) {
         rows_pad = rows_pad_of(bd.nrows);
-        rr = t % rows_pad;
-        valid = rr < bd.nrows;
-        if (rows_pad <= 32) {          // 32 / rows_pad copies per warp, 16 key columns per warp
+        rr = pos >= 0 ? pos % rows_pad : 0;
+        valid = pos >= 0 && rr < bd.nrows;
+        // copy c = pos / rows_pad of a row owns key columns [c*len, (c+1)*len) of
+        // every tile; a warp reads the columns of the copies it holds
+        constexpr int ppw = kRows / 4;           // row positions per warp
+        len = kN * rows_pad / kRows;
+        if (rows_pad <= ppw) {                   // several copies per warp: 16 columns
           nc = 16;
           col0 = 16 * warp;
-          len = rows_pad / 2;
-          off = (t / rows_pad) * len - col0;
-        } else if (rows_pad == 64) {   // two copies, 32 key columns each
-          nc = 32;
-          col0 = 32 * (warp >> 1);
-          len = 32;
-          off = 0;
-        } else {
-          nc = kN;
-          col0 = 0;
-          len = kN;
+          off = (pos >= 0 ? pos / rows_pad : 0) * len - col0;
+        } else {                                 // part of one copy per warp
+          nc = len;
+          col0 = ((warp * ppw) / rows_pad) * len;
           off = 0;
         }
         warp_live = __any_sync(0xffffffffu, valid);
@@ -712,11 +721,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const SegDesc &sd = cur.sd;
       const bool single = bd.num_splits == 1;
       if (rows_pad == kRows) {
-        // one copy per row: thread t owns row t outright
+        // one copy per row: the thread owns its row position outright
         if (warp_live) {
           int tok = 0, h = 0;
           if (valid) {
-            const int flat = bd.row0 + t;
+            const int flat = bd.row0 + pos;
             tok = bd.tok0 + flat / a.group;
             h = bd.g * a.group + flat % a.group;
           }
@@ -733,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             scale_o = l_run > 0.f ? a.v_scale / l_run : 0.f;
             lse = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
           }
-          const int prow = bd.part_row_base + sd.split * bd.nrows + t;
+          const int prow = bd.part_row_base + sd.split * bd.nrows + pos;
 #pragma unroll
           for (int c = 0; c < kDv / 32; ++c) {
             uint32_t o[32];
@@ -776,8 +785,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // copy at a time, scaled to the row's common max (stride 33: no bank
         // conflicts); each thread then sums the copies of (row, column) pairs.
         const int copies = kRows / rows_pad;
-        sm_m[t] = valid ? m_run : -INFINITY;
-        sm_l[t] = valid ? l_run : 0.f;
+        if (pos >= 0) {
+          sm_m[pos] = valid ? m_run : -INFINITY;
+          sm_l[pos] = valid ? l_run : 0.f;
+        }
         if (!group_sync()) break;
         float f = 0.f;
         if (valid && m_run != -INFINITY) {
@@ -795,7 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) buf[t * 33 + j] = valid ? f * __uint_as_float(o[j]) : 0.f;
+            if (pos >= 0)
+              for (int j = 0; j < 32; ++j) buf[pos * 33 + j] = valid ? f * __uint_as_float(o[j]) : 0.f;
           }
           sync_ok = group_sync() && sync_ok;
 #pragma unroll 1
@@ -850,16 +862,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool FP8, bool TMA>
+template <bool FP8, bool TMA, int MR>
 cudaError_t launch_one(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
-  attn_tc_kernel<FP8, TMA><<<hp.num_ctas, kThreads, Layout<FP8>::kSmem, st>>>(a, m);
+  attn_tc_kernel<FP8, TMA, MR><<<hp.num_ctas, kThreads, Layout<FP8, MR>::kSmem, st>>>(a, m);
   return cudaGetLastError();
 }
 
-template <bool FP8, bool TMA>
+template <bool FP8, bool TMA, int MR>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(attn_tc_kernel<FP8, TMA>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<FP8>::kSmem);
+  return cudaFuncSetAttribute(attn_tc_kernel<FP8, TMA, MR>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<FP8, MR>::kSmem);
+}
+
+template <int MR>
+cudaError_t launch_rows(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
+  const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
+  if (hp.use_tma)
+    return fp8 ? launch_one<true, true, MR>(hp, a, m, st) : launch_one<false, true, MR>(hp, a, m, st);
+  return fp8 ? launch_one<true, false, MR>(hp, a, m, st) : launch_one<false, false, MR>(hp, a, m, st);
+}
+
+template <int MR>
+cudaError_t prepare_rows(const HostPlan &hp) {
+  const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
+  if (hp.use_tma) return fp8 ? prepare_one<true, true, MR>() : prepare_one<false, true, MR>();
+  return fp8 ? prepare_one<true, false, MR>() : prepare_one<false, false, MR>();
 }
 
 }  // namespace
@@ -872,16 +899,12 @@ bool tc_tma_page_size(int32_t page_size, int32_t num_pages) {
 cudaError_t launch_attn_tc(const HostPlan &hp, const RunArgs &a, const TmaMaps &m,
                            cudaStream_t stream) {
   if (hp.num_ctas == 0) return cudaSuccess;
-  const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
-  if (hp.use_tma)
-    return fp8 ? launch_one<true, true>(hp, a, m, stream) : launch_one<false, true>(hp, a, m, stream);
-  return fp8 ? launch_one<true, false>(hp, a, m, stream) : launch_one<false, false>(hp, a, m, stream);
+  return hp.block_rows == 64 ? launch_rows<64>(hp, a, m, stream)
+                             : launch_rows<128>(hp, a, m, stream);
 }
 
 cudaError_t prepare_attn_tc(const HostPlan &hp) {
-  const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
-  if (hp.use_tma) return fp8 ? prepare_one<true, true>() : prepare_one<false, true>();
-  return fp8 ? prepare_one<true, false>() : prepare_one<false, false>();
+  return hp.block_rows == 64 ? prepare_rows<64>(hp) : prepare_rows<128>(hp);
 }
 
 }  // namespace akp

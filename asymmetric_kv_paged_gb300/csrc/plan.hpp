@@ -13,10 +13,10 @@ constexpr int kDqk = 192;       // query/key head dim
 constexpr int kDv = 128;        // value head dim
 constexpr int kKeyTile = 64;    // keys per pipeline tile
 
-// Query rows per row block.  A block packs up to 128 query rows of one
+// Query rows per row block.  A block packs up to block_rows query rows of one
 // (request, KV head): row r <-> (token r / G, head g*G + r % G); decode blocks
-// hold G rows, verify blocks n*G, prefill blocks 128.
-constexpr int32_t kBlockRows = 128;
+// hold G rows, verify blocks n*G, prefill blocks 128.  block_rows is 64 (M=64
+// MMAs) when no (request, KV head) has more than 64 query rows, else 128.
 
 // One row block: rows [row0, row0 + nrows) of (b, g).  Keys [klo, khi) are
 // the union of what its rows can see.
@@ -43,6 +43,7 @@ struct HostPlan {
   attn_problem_t prob{};
   std::vector<int32_t> qo_indptr, seq_lens;
   int32_t group = 1;             // G = Hq / Hkv
+  int32_t block_rows = 128;      // 64 or 128 (the MMA M)
   int32_t num_sms = 0, num_ctas = 0, threads = 0;
   std::vector<BlockDesc> blocks;
   std::vector<SegDesc> segs;

@@ -51,7 +51,11 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
     return ATTN_ERR_UNSUPPORTED;
 
   hp.threads = 320;
-  const int32_t rows_per_block = kBlockRows;
+  int64_t max_rows = 0;
+  for (int32_t b = 0; b < p->batch; ++b)
+    max_rows = std::max<int64_t>(max_rows, (int64_t)(hp.qo_indptr[b + 1] - hp.qo_indptr[b]) * hp.group);
+  hp.block_rows = max_rows <= 64 ? 64 : 128;
+  const int32_t rows_per_block = hp.block_rows;
   const int32_t G = hp.group;
 
   // Row blocks.

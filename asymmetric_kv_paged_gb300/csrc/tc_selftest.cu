@@ -52,6 +52,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (mode == 0) {
     stage_sw128(sa, a, 128, 192);   // [128 x 192] K-major
     stage_sw128(sb, b, n, 192);     // [n x 192] K-major
+  } else if (mode == 2) {
+    stage_sw128(sa, a, 64, 192);    // [64 x 192] K-major
+    stage_sw128(sb, b, 64, 192);    // [64 x 192] K-major
   } else {
     stage_sw128(sa, a, 128, 64);    // [128 x 64] K-major
     stage_sw128(sb, b, 64, 128);    // [64 keys x 128] stored key-major: MN-major B
@@ -73,6 +76,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd = tc::smem_desc_sw128(b0 + (ks / 4) * n * 128 + koff, 16, 1024);
         tc::mma_f16_ss(tmem, ad, bd, idesc, ks > 0);
       }
+    } else if (mode == 2) {
+      const uint32_t idesc = tc::idesc_f16(ab_type, 0, 0, 64, 64);
+      for (int ks = 0; ks < 12; ++ks) {
+        const uint32_t koff = (ks % 4) * 32u;
+        const uint64_t ad = tc::smem_desc_sw128(a0 + (ks / 4) * 64 * 128 + koff, 16, 1024);
+        const uint64_t bd = tc::smem_desc_sw128(b0 + (ks / 4) * 64 * 128 + koff, 16, 1024);
+        tc::mma_f16_ss(tmem, ad, bd, idesc, ks > 0);
+      }
     } else {
       const uint32_t idesc = tc::idesc_f16(ab_type, 0, 1, 128, 128);
       const uint32_t lbo = variant == 0 ? 64 * 128 : 1024;   // between 64-wide N blocks
@@ -87,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const bool ok = tc::mbar_wait(&bar, 0, &abort_flag);
   tc::tc_fence_after();
-  const int ncols = mode == 0 ? n : 128;
+  const int ncols = mode == 0 ? n : (mode == 2 ? 64 : 128);
   if (ok) {
     const int row = threadIdx.x;   // TMEM lane = row; warp w owns lanes 32w..32w+31
     for (int c0 = 0; c0 < ncols; c0 += 32) {
@@ -110,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 extern "C" attn_status_t attn_debug_tc_gemm(int32_t mode, int32_t variant, int32_t ab_type,
                                             int32_t n, const void *a, const void *b, float *d,
                                             int32_t *status, void *stream) {
-  if (mode != 0 && mode != 1) return ATTN_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 2) return ATTN_ERR_INVALID_ARG;
   if (mode == 0 && n != 64 && n != 128) return ATTN_ERR_INVALID_ARG;
   if (variant != 0 && variant != 1) return ATTN_ERR_INVALID_ARG;
   if (ab_type != 0 && ab_type != 1) return ATTN_ERR_INVALID_ARG;

@@ -22,7 +22,10 @@ extern "C" {
  *   mode 1: d[128 x 128] = a[128 x 64] * b[64 x 128]
  *           (b stored row-major, i.e. MN-major, as V in P.V); variant 0/1
  *           picks which descriptor offset spans the two 64-wide column blocks
- *           of b (0: leading offset, 1: stride offset).
+ *           of b (0: leading offset, 1: stride offset);
+ *   mode 2: the M=64 form: a[64 x 192] * b[64 x 192]^T; d receives all 128
+ *           TMEM lanes x 64 columns as d[128 x 64], so the test can check
+ *           which lanes hold the 64 rows (unused lanes hold whatever TMEM had).
  * a, b: device 16-bit matrices, row-major (ab_type 0 = fp16, 1 = bf16);
  * d: device fp32, row-major; status: device int32, set to 1 if the
  * completion wait timed out (left untouched otherwise).  Asynchronous on

@@ -44,3 +44,28 @@ def test_pv_shape_mnmajor(ab_type):
         errs.append((d - ref).abs().max().item())
     tol = 1e-3 * ref.abs().max().item()
     assert errs[0] < tol, f"leading-offset variant err {errs[0]:.3g}, stride variant {errs[1]:.3g}"
+
+
+def test_m64_accumulator_lanes():
+    """An M=64 product lands in TMEM lanes 0-15 of each 32-lane subpartition:
+    row r in lane 32*(r//16) + r%16 (the layout the attention kernel reads)."""
+    import numpy as np
+    g = torch.Generator(device="cuda").manual_seed(3)
+    a = torch.randn(64, 192, device="cuda", generator=g).to(torch.bfloat16)
+    b = torch.randn(64, 192, device="cuda", generator=g).to(torch.bfloat16)
+    from asymmetric_kv_paged_gb300 import binding as B
+    d = torch.zeros((128, 64), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.attn_debug_tc_gemm(2, 0, 1, 64, a, b, d, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = (a.float() @ b.float().T).cpu().numpy()
+    got = d.cpu().numpy()
+    tol = 1e-3 * np.abs(ref).max()
+    found = {}
+    for lane in range(128):
+        for r in range(64):
+            if np.all(np.isfinite(got[lane])) and np.abs(got[lane] - ref[r]).max() < tol:
+                found[r] = lane
+    expect = {r: 32 * (r // 16) + r % 16 for r in range(64)}
+    assert found == expect, f"row -> lane map: {sorted(found.items())}"
