@@ -452,11 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp.init(a.segs, a.blocks, seg_begin, seg_end);
       int ks = 0, kp = 0;
       uint64_t idle_since = 0;
+      uint32_t idle_polls = 0;
       // BF16 + TMA: interior tiles are consumed straight off the TMA barrier;
       // edge tiles wait for the converters, whose barrier then completes only
       // on edge tiles (one parity bit per stage).
       uint32_t edge_parity = 0, inner_parity = 0;
-      constexpr uint32_t kPoll = 64;   // ns of hardware sleep per barrier probe
       while (kp < total) {
         bool progressed = false;
         if (kp < ks) {
@@ -464,9 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = kp % NS;
           const bool first = cp.first();
           const bool ready =
-              tc::mbar_try_wait(tc::smem_u32(&bars.p_full[b]), (kp >> 1) & 1, kPoll) &&
+              tc::mbar_test_wait(tc::smem_u32(&bars.p_full[b]), (kp >> 1) & 1) &&
               (!first || cp.si == 0 ||
-               tc::mbar_try_wait(tc::smem_u32(&bars.o_free), (cp.si - 1) & 1, kPoll));
+               tc::mbar_test_wait(tc::smem_u32(&bars.o_free), (cp.si - 1) & 1));
           if (ready) {
             tc::tc_fence_after();
             const uint32_t pb = sbase + Lay::kOffP + b * kPBytes;
@@ -489,17 +489,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = ks & 1;
           const int key0 = cs.tile * kN;
           const bool edge = !(TMA && !FP8) || key0 < cs.bd.klo || key0 + kN > cs.bd.khi;
-          const bool land = edge ? tc::mbar_try_wait(tc::smem_u32(&bars.op_full[s]),
+          const bool land = edge ? tc::mbar_test_wait(tc::smem_u32(&bars.op_full[s]),
                                                      (TMA && !FP8) ? (edge_parity >> s) & 1
-                                                                   : (ks / NS) & 1,
-                                                     kPoll)
-                                 : tc::mbar_try_wait(tc::smem_u32(&bars.tma_full[s]),
-                                                     (inner_parity >> s) & 1, kPoll);
+                                                                   : (ks / NS) & 1)
+                                 : tc::mbar_test_wait(tc::smem_u32(&bars.tma_full[s]),
+                                                      (inner_parity >> s) & 1);
           const bool ready =
-              (!cs.first() || tc::mbar_try_wait(tc::smem_u32(&bars.q_full), cs.si & 1, kPoll)) &&
+              (!cs.first() || tc::mbar_test_wait(tc::smem_u32(&bars.q_full), cs.si & 1)) &&
               land &&
               (ks < 2 ||
-               tc::mbar_try_wait(tc::smem_u32(&bars.s_empty[b]), ((ks >> 1) - 1) & 1, kPoll));
+               tc::mbar_test_wait(tc::smem_u32(&bars.s_empty[b]), ((ks >> 1) - 1) & 1));
           if (ready) {
             if (TMA && !FP8) {
               if (edge)
@@ -525,8 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (progressed) {
           idle_since = 0;
-        } else {
-          // bounded like every other wait: give up after 2 s without progress
+          idle_polls = 0;
+        } else if ((++idle_polls & 255u) == 0) {
+          // bounded like every other wait: give up after 2 s without progress.
+          // The timer is read only every 256 empty polls: the read is slow
+          // enough to delay the next issue noticeably.
           if (abort_flag) break;
           const uint64_t now = tc::globaltimer_ns();
           if (idle_since == 0) {
@@ -553,120 +555,161 @@ __global__ void __launch_bounds__(kThreads, 1)
     cur.init(a.segs, a.blocks, seg_begin, seg_end);
     float m_run = -INFINITY, l_run = 0.f;
     int row_lo = 0, row_hi = 0, rr = 0, rows_pad = kRows, col0 = 0, off = 0, len = kN, nc = kN;
+    int zero_pending = 0;
     bool valid = false, warp_live = false;
     uint32_t sync_phase = 0;
+    // Bounded wait with a warp-uniform outcome: the TMEM loads that follow are
+    // warp-collective, so a warp must never split on a give-up.
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity, &abort_flag));
+    };
     // bounded rendezvous of the 128 softmax threads
     auto group_sync = [&]() -> bool {
       tc::mbar_arrive(&bars.sm_sync);
-      const bool ok = tc::mbar_wait(&bars.sm_sync, sync_phase, &abort_flag);
+      const bool ok = wait(&bars.sm_sync, sync_phase);
       sync_phase ^= 1;
       return ok;
     };
-    // one key tile: S slice from TMEM -> mask -> running max -> P slice to smem.
-    // NC key columns per thread (16, 32 or 64).  The 64-column case reads S
-    // from TMEM twice (max pass, then exp pass) to keep register use low.
-    auto tile_body = [&](auto nc_tag, int k) -> bool {
-      constexpr int NC = decltype(nc_tag)::value;
-      constexpr int NH = NC > 32 ? 32 : NC;     // columns held in registers at a time
+    // One key tile: S slice from TMEM -> mask -> P slice to smem.
+    // A thread owns nc (16, 32 or 64) key columns of its row, read from TMEM in
+    // 16-column chunks; the load of chunk c+1 is in flight while chunk c is
+    // processed.  The loops are not unrolled beyond that pair, so this hot code
+    // stays small: each SM sub-partition's instruction cache also holds the
+    // converter and MMA loops, and a fully unrolled 64-column body thrashes it.
+    //
+    // P is computed against the running maximum m_run in a single pass over S,
+    // tracking the tile maximum on the way.  Only when some value exceeds
+    // m_run by more than the rescale threshold (rare once the maximum has
+    // settled) is O rescaled and the pass repeated against the new maximum.
+    // The first tile of a segment (m_run = -inf) takes a max pass first.
+    auto scaled16 = [&](const uint32_t (&raw)[16], int c, int j_lo, int j_hi, float (&v)[16]) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int jj = 16 * c + j;
+        const bool in = (jj >= j_lo) & (jj < j_hi);
+        v[j] = in ? __uint_as_float(raw[j]) * a.scale_log2 : -INFINITY;
+      }
+    };
+    auto tile_body = [&](int k) -> bool {
       const int b = k & 1;
-      // visible columns of this thread in the warp's NC-column window: its own
+      // visible columns of this thread in the warp's nc-column window: its own
       // slice [off, off + len) clipped to the row's keys [row_lo, row_hi)
       const int key0 = cur.tile * kN + col0;
       const int j_lo = max(off, row_lo - key0);
       const int j_hi = min(off + len, row_hi - key0);
-      auto load_scaled = [&](int q, float (&v)[NH]) {
-        uint32_t raw[NH];
-        if constexpr (NH == 16)
-          tc::tmem_ld16(tmem + lane_base + b * kN + col0, raw);
-        else
-          tc::tmem_ld32(tmem + lane_base + b * kN + col0 + 32 * q, raw);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < NH; ++j) {
-          const int jj = q * NH + j;
-          const bool in = (jj >= j_lo) & (jj < j_hi);
-          v[j] = in ? __uint_as_float(raw[j]) * a.scale_log2 : -INFINITY;
-        }
-      };
+      const uint32_t taddr = tmem + lane_base + b * kN + col0;
+      const int nch = nc >> 4;
+      // P buffer b is free once P.V of tile k-2 is done
+      if (k >= 2 && !wait(&bars.pv_done[b], ((k - 2) >> 1) & 1))
+        return false;
       if (!warp_live) {
         tc::tc_fence_before();
         tc::mbar_arrive(&bars.s_empty[b]);
-        if (k >= 2 && !tc::mbar_wait(&bars.pv_done[b], ((k - 2) >> 1) & 1, &abort_flag))
-          return false;
         return true;
       }
-      float v[NH];
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int q = 0; q < NC / NH; ++q) {
-        load_scaled(q, v);
-#pragma unroll
-        for (int j = 0; j < NH; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
-      }
-      if constexpr (NC == NH) {      // values stay in registers: S may be reused now
-        tc::tc_fence_before();
-        tc::mbar_arrive(&bars.s_empty[b]);
-      }
-      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      if (cur.first()) {
-        m_run = m_tile;
-        l_run = 0.f;
-      } else {
-        const bool need = m_tile > m_run + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          if (!tc::mbar_wait(&bars.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, &abort_flag))
-            return false;
-          tc::tc_fence_after();
-          const float m_new = need ? m_tile : m_run;
-          const float alpha = need ? ex2(m_run - m_new) : 1.f;
+      uint32_t ra[16], rb[16];
+      float v[16];
+      // The TMEM loads are warp-collective: the whole warp takes the max pass
+      // when any of its rows needs it, and only those rows adopt its result.
+      const bool want_max = valid && (cur.first() || m_run == -INFINITY);
+      if (__any_sync(0xffffffffu, want_max)) {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        tc::tmem_ld16(taddr, ra);
+        tc::tmem_wait_ld_regs(ra);
 #pragma unroll 1
-          for (int c = 0; c < kDv / 32; ++c) {
-            uint32_t o[32];
-            tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
-            tc::tmem_wait_ld();
+        for (int c = 0; c < nch; c += 2) {
+          if (c + 1 < nch) tc::tmem_ld16(taddr + 16 * (c + 1), rb);
+          scaled16(ra, c, j_lo, j_hi, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tc::tmem_st32(tmem + lane_base + kTmemO + c * 32, o);
+          for (int j = 0; j < 16; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+          if (c + 1 < nch) {
+            tc::tmem_wait_ld_regs(rb);
+            if (c + 2 < nch) tc::tmem_ld16(taddr + 16 * (c + 2), ra);
+            scaled16(rb, c + 1, j_lo, j_hi, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+            if (c + 2 < nch) tc::tmem_wait_ld_regs(ra);
           }
-          tc::tmem_wait_st();
-          l_run *= alpha;
-          m_run = m_new;
         }
+        if (want_max) m_run = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       }
-      const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      if (k >= 2 && !tc::mbar_wait(&bars.pv_done[b], ((k - 2) >> 1) & 1, &abort_flag))
-        return false;
       uint8_t *prow = smem + Lay::kOffP + b * kPBytes;
       const int ch0 = col0 >> 3;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      if (zero_pending > 0) {
+        // P columns outside the window stay zero for the whole segment: write
+        // them once per buffer (the first two tiles), not on every tile
+        --zero_pending;
+        if (pos >= 0)
+#pragma unroll 1
+          for (int ch = 0; ch < 8; ++ch)
+            if (ch < ch0 || ch >= ch0 + 2 * nch)
+              *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      // exp pass over chunk c held in raw: P to smem, sums and maximum
+      float rs[4], mx[4];
+      const auto exp16 = [&](const uint32_t (&raw)[16], int c, float m_use) {
+        scaled16(raw, c, j_lo, j_hi, v);
+        uint32_t pk[8];
 #pragma unroll
-      for (int q = 0; q < NC / NH; ++q) {
-        if (NC != NH) load_scaled(q, v);
-        uint32_t pk[NH / 2];
-#pragma unroll
-        for (int j = 0; j < NH; j += 2) {
+        for (int j = 0; j < 16; j += 2) {
+          mx[(j >> 1) & 3] = fmaxf(mx[(j >> 1) & 3], fmaxf(v[j], v[j + 1]));
           const float p0 = ex2(v[j] - m_use);
           const float p1 = ex2(v[j + 1] - m_use);
           rs[(j >> 1) & 3] += p0 + p1;
           pk[j / 2] = cvt_pair(p0, p1, kHalf);
         }
+        if (pos >= 0) {
+          *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch0 + 2 * c)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch0 + 2 * c + 1)) =
+              make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      };
+#pragma unroll 1
+      for (int pass = 0;; ++pass) {
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
-        for (int i = 0; i < NH / 8; ++i)
-          if (pos >= 0)
-            *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch0 + q * (NH / 8) + i)) =
-              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int i = 0; i < 4; ++i) {
+          rs[i] = 0.f;
+          mx[i] = -INFINITY;
+        }
+        tc::tmem_ld16(taddr, ra);
+        tc::tmem_wait_ld_regs(ra);
+#pragma unroll 1
+        for (int c = 0; c < nch; c += 2) {
+          if (c + 1 < nch) tc::tmem_ld16(taddr + 16 * (c + 1), rb);
+          exp16(ra, c, m_use);
+          if (c + 1 < nch) {
+            tc::tmem_wait_ld_regs(rb);
+            if (c + 2 < nch) tc::tmem_ld16(taddr + 16 * (c + 2), ra);
+            exp16(rb, c + 1, m_use);
+            if (c + 2 < nch) tc::tmem_wait_ld_regs(ra);
+          }
+        }
+        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const bool need = m_tile > m_run + kRescaleThreshold;
+        if (pass > 0 || !__any_sync(0xffffffffu, need)) break;
+        // rare: the maximum grew past the threshold; rescale O and redo
+        if (!wait(&bars.pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1))
+          return false;
+        tc::tc_fence_after();
+        const float alpha = need ? ex2(m_run - m_tile) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < kDv / 32; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tc::tmem_st32(tmem + lane_base + kTmemO + c * 32, o);
+        }
+        tc::tmem_wait_st();
+        l_run *= alpha;
+        if (need) m_run = m_tile;
       }
-      if constexpr (NC != NH) {      // second TMEM pass done: S may be reused now
-        tc::tc_fence_before();
-        tc::mbar_arrive(&bars.s_empty[b]);
-      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars.s_empty[b]);
       l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      if constexpr (NC < kN) {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          if (pos >= 0 && (ch < ch0 || ch >= ch0 + NC / 8))
-            *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch)) = make_uint4(0u, 0u, 0u, 0u);
-      }
       tc::fence_proxy_async_smem();
       return true;
     };
@@ -699,24 +742,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m_run = -INFINITY;
         l_run = 0.f;
+        zero_pending = nc < kN ? 2 : 0;
       }
       const int b = k & 1;
-      if (!tc::mbar_wait(&bars.s_full[b], (k >> 1) & 1, &abort_flag)) break;
+      if (!wait(&bars.s_full[b], (k >> 1) & 1)) break;
       tc::tc_fence_after();
-      bool ok;
-      if (nc == 16)
-        ok = tile_body(std::integral_constant<int, 16>{}, k);
-      else if (nc == 32)
-        ok = tile_body(std::integral_constant<int, 32>{}, k);
-      else
-        ok = tile_body(std::integral_constant<int, 64>{}, k);
-      if (!ok) break;
+      if (!tile_body(k)) break;
       tc::tc_fence_before();
       tc::mbar_arrive(&bars.p_full[b]);
       if (!cur.last()) continue;
 
       // ---------------- end of segment: normalise and write the block's rows
-      if (!tc::mbar_wait(&bars.pv_done[b], (k >> 1) & 1, &abort_flag)) break;
+      if (!wait(&bars.pv_done[b], (k >> 1) & 1)) break;
       tc::tc_fence_after();
       const SegDesc &sd = cur.sd;
       const bool single = bd.num_splits == 1;
@@ -805,8 +842,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[32];
             tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
             tc::tmem_wait_ld();
-#pragma unroll
             if (pos >= 0)
+#pragma unroll
               for (int j = 0; j < 32; ++j) buf[pos * 33 + j] = valid ? f * __uint_as_float(o[j]) : 0.f;
           }
           sync_ok = group_sync() && sync_ok;
