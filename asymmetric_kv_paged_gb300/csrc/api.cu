@@ -175,6 +175,9 @@ static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const
   if ((sinks != nullptr) != (pr.has_sinks != 0)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return ATTN_ERR_INVALID_ARG;
+  // the kernels take score maxima on unscaled dot products: the scale must be > 0
+  if (!(softmax_scale > 0.f) || (pr.kv_dtype == ATTN_KV_FP8_E4M3 && !(k_scale > 0.f)))
+    return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < hp.workspace_bytes || (hp.workspace_bytes && !workspace))
     return ATTN_ERR_WORKSPACE;
   if (!has_rows) return ATTN_OK;

@@ -582,12 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // m_run by more than the rescale threshold (rare once the maximum has
     // settled) is O rescaled and the pass repeated against the new maximum.
     // The first tile of a segment (m_run = -inf) takes a max pass first.
-    auto scaled16 = [&](const uint32_t (&raw)[16], int c, int j_lo, int j_hi, float (&v)[16]) {
+    // Columns outside the thread's visible range read as -inf.  The score
+    // scale is positive (the entry points reject anything else), so maxima are
+    // taken on the raw dot products and -inf stays -inf once scaled.
+    auto mask16 = [&](uint32_t (&raw)[16], int c, int j_lo, int j_hi) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int jj = 16 * c + j;
-        const bool in = (jj >= j_lo) & (jj < j_hi);
-        v[j] = in ? __uint_as_float(raw[j]) * a.scale_log2 : -INFINITY;
+        raw[j] = ((jj >= j_lo) & (jj < j_hi)) ? raw[j] : 0xFF800000u;
       }
     };
     auto tile_body = [&](int k) -> bool {
@@ -599,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j_hi = min(off + len, row_hi - key0);
       const uint32_t taddr = tmem + lane_base + b * kN + col0;
       const int nch = nc >> 4;
+      const float sc = a.scale_log2;
       // P buffer b is free once P.V of tile k-2 is done
       if (k >= 2 && !wait(&bars.pv_done[b], ((k - 2) >> 1) & 1))
         return false;
@@ -607,31 +610,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(&bars.s_empty[b]);
         return true;
       }
+      // interior tiles (every column of every thread visible) skip the mask
+      const bool full = __all_sync(0xffffffffu, j_lo <= 0 && j_hi >= nc);
       uint32_t ra[16], rb[16];
-      float v[16];
       // The TMEM loads are warp-collective: the whole warp takes the max pass
       // when any of its rows needs it, and only those rows adopt its result.
       const bool want_max = valid && (cur.first() || m_run == -INFINITY);
       if (__any_sync(0xffffffffu, want_max)) {
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        tc::tmem_ld16(taddr, ra);
-        tc::tmem_wait_ld_regs(ra);
 #pragma unroll 1
-        for (int c = 0; c < nch; c += 2) {
-          if (c + 1 < nch) tc::tmem_ld16(taddr + 16 * (c + 1), rb);
-          scaled16(ra, c, j_lo, j_hi, v);
+        for (int c = 0; c < nch; ++c) {
+          tc::tmem_ld16(taddr + 16 * c, ra);
+          tc::tmem_wait_ld_regs(ra);
+          mask16(ra, c, j_lo, j_hi);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
-          if (c + 1 < nch) {
-            tc::tmem_wait_ld_regs(rb);
-            if (c + 2 < nch) tc::tmem_ld16(taddr + 16 * (c + 2), ra);
-            scaled16(rb, c + 1, j_lo, j_hi, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
-            if (c + 2 < nch) tc::tmem_wait_ld_regs(ra);
-          }
+          for (int j = 0; j < 16; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
         }
-        if (want_max) m_run = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        if (want_max) m_run = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
       }
       uint8_t *prow = smem + Lay::kOffP + b * kPBytes;
       const int ch0 = col0 >> 3;
@@ -645,16 +640,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ch < ch0 || ch >= ch0 + 2 * nch)
               *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch)) = make_uint4(0u, 0u, 0u, 0u);
       }
-      // exp pass over chunk c held in raw: P to smem, sums and maximum
+      // exp pass over chunk c held in raw: P = 2^(s * sc - m) to smem, row sums
+      // and the raw maximum
       float rs[4], mx[4];
-      const auto exp16 = [&](const uint32_t (&raw)[16], int c, float m_use) {
-        scaled16(raw, c, j_lo, j_hi, v);
+      const auto exp16 = [&](uint32_t (&raw)[16], int c, float neg_m) {
+        if (!full) mask16(raw, c, j_lo, j_hi);
         uint32_t pk[8];
 #pragma unroll
         for (int j = 0; j < 16; j += 2) {
-          mx[(j >> 1) & 3] = fmaxf(mx[(j >> 1) & 3], fmaxf(v[j], v[j + 1]));
-          const float p0 = ex2(v[j] - m_use);
-          const float p1 = ex2(v[j + 1] - m_use);
+          const float x0 = __uint_as_float(raw[j]), x1 = __uint_as_float(raw[j + 1]);
+          mx[(j >> 1) & 3] = fmaxf(mx[(j >> 1) & 3], fmaxf(x0, x1));
+          const float p0 = ex2(fmaf(x0, sc, neg_m));
+          const float p1 = ex2(fmaf(x1, sc, neg_m));
           rs[(j >> 1) & 3] += p0 + p1;
           pk[j / 2] = cvt_pair(p0, p1, kHalf);
         }
@@ -667,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 #pragma unroll 1
       for (int pass = 0;; ++pass) {
-        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           rs[i] = 0.f;
@@ -678,15 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < nch; c += 2) {
           if (c + 1 < nch) tc::tmem_ld16(taddr + 16 * (c + 1), rb);
-          exp16(ra, c, m_use);
+          exp16(ra, c, neg_m);
           if (c + 1 < nch) {
             tc::tmem_wait_ld_regs(rb);
             if (c + 2 < nch) tc::tmem_ld16(taddr + 16 * (c + 2), ra);
-            exp16(rb, c + 1, m_use);
+            exp16(rb, c + 1, neg_m);
             if (c + 2 < nch) tc::tmem_wait_ld_regs(ra);
           }
         }
-        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
         const bool need = m_tile > m_run + kRescaleThreshold;
         if (pass > 0 || !__any_sync(0xffffffffu, need)) break;
         // rare: the maximum grew past the threshold; rescale O and redo

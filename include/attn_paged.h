@@ -125,7 +125,8 @@ attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *
  *                NULL; must be non-NULL exactly when the plan has_sinks.
  *   window       must equal the plan's window.
  *   softmax_scale, k_scale, v_scale  as in the operation above (the kv scales
- *                are ignored for bf16 caches and should be 1).
+ *                are ignored for bf16 caches and should be 1).  All finite;
+ *                softmax_scale > 0, and k_scale > 0 for an FP8 cache.
  *   out          bf16 [total_q, Hq, 128].
  *   lse_out      fp32 [total_q, Hq] natural-log denominators, or NULL.
  *   workspace    device scratch of at least workspace_bytes (may be NULL when

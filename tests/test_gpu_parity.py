@@ -164,7 +164,9 @@ def test_run_argument_errors():
     for upd, status in [(dict(window=65), B.ATTN_ERR_INVALID_ARG),
                         (dict(sinks=None), B.ATTN_ERR_INVALID_ARG),
                         (dict(q=None), B.ATTN_ERR_INVALID_ARG),
-                        (dict(softmax_scale=float("nan")), B.ATTN_ERR_INVALID_ARG)]:
+                        (dict(softmax_scale=float("nan")), B.ATTN_ERR_INVALID_ARG),
+                        (dict(softmax_scale=-w.softmax_scale), B.ATTN_ERR_INVALID_ARG),
+                        (dict(softmax_scale=0.0), B.ATTN_ERR_INVALID_ARG)]:
         with pytest.raises(B.AttnError) as e:
             B.attn_run_paged(**dict(base, **upd))
         assert e.value.status == status
