@@ -10,17 +10,18 @@
 // than 128 rows (decode: G rows) still issue M=128 MMAs: the tensor pipe has
 // time to spare while the tile streams in from HBM.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-3  softmax + epilogue: thread r owns row r (= TMEM lane r);
 //   warps 4-7  converters: stage Q per block; turn raw FP8 K/V tiles into
 //              exact fp16 operand tiles; zero V rows of keys outside the
 //              block's range on edge tiles (unused slots may hold NaN:
 //              sammysun0711/sglang PR #35, FlyPA V-tail masking); or, for
 //              page sizes TMA cannot tile, gather K/V rows themselves;
-//   warp  8    TMEM allocation and every tcgen05.mma (one thread);
+//   warp  8    TMEM allocation; issues the S = Q.K^T MMAs (one thread);
 //   warp  9    TMA producer: page-table lookup, then 3D tensor-map loads of
 //              the K/V boxes (BF16: straight into the 128-byte swizzled
-//              operand layout; FP8: raw rows into a staging ring).
+//              operand layout; FP8: raw rows into a staging ring);
+//   warp 10    issues the O += P.V MMAs (one thread).
 // TMEM: S double buffer (2 x 64 columns) + O (128 columns).
 // Every wait is bounded in time; a broken invariant ends the kernel with bit 1
 // of the plan's error word set instead of hanging the GPU.
@@ -39,7 +40,7 @@ namespace akp {
 namespace {
 
 constexpr int kN = kKeyTile;                 // keys per tile (64)
-constexpr int kThreads = 10 * 32;
+constexpr int kThreads = 11 * 32;
 constexpr int kBlk = kN * 128;               // one 64-column block of a 64-row tile: 8 KB
 constexpr int kOpK = 3 * kBlk;               // K operand tile: 24 KB
 constexpr int kOpBytes = kOpK + 2 * kBlk;    // + V operand tile: 40 KB
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars.pv_done[b], 1);
     }
     tc::mbar_init(&bars.o_free, 128);
-    tc::mbar_init(&bars.final_done, 1);
+    tc::mbar_init(&bars.final_done, 2);
     tc::mbar_init(&bars.sm_sync, 128);
     tc::fence_mbar_init();
   }
@@ -440,104 +441,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_arrive(&bars.op_full[s]);
     }
   } else if (warp == 8) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S = Q.K^T issuer
+    // One thread issues every Q.K^T MMA, in tile order.  P.V goes out from a
+    // thread of its own (warp 10): an MMA issue blocks the issuing thread for
+    // as long as the tensor pipe takes to accept it, so with one issuer P.V of
+    // tile k would queue behind the whole Q.K^T of tile k+1.
     if ((tid & 31) == 0) {
       const uint32_t id_s = tc::idesc_f16(kHalf ? 0 : 1, 0, 0, kRows, kN);
-      const uint32_t id_pv = tc::idesc_f16(kHalf ? 0 : 1, 0, 1, kRows, kDv);
-      // Two streams of work, S = Q.K^T per tile and O += P.V per tile, issued in
-      // tile order each but interleaved by readiness: P.V of tile k goes out as
-      // soon as its P is written, without waiting for tile k+1's K to land.
-      Cursor cs, cp;
+      Cursor cs;
       cs.init(a.segs, a.blocks, seg_begin, seg_end);
-      cp.init(a.segs, a.blocks, seg_begin, seg_end);
-      int ks = 0, kp = 0;
-      uint64_t idle_since = 0;
-      uint32_t idle_polls = 0;
       // BF16 + TMA: interior tiles are consumed straight off the TMA barrier;
       // edge tiles wait for the converters, whose barrier then completes only
       // on edge tiles (one parity bit per stage).
       uint32_t edge_parity = 0, inner_parity = 0;
-      while (kp < total) {
-        bool progressed = false;
-        if (kp < ks) {
-          const int b = kp & 1;
-          const int s = kp % NS;
-          const bool first = cp.first();
-          const bool ready =
-              tc::mbar_test_wait(tc::smem_u32(&bars.p_full[b]), (kp >> 1) & 1) &&
-              (!first || cp.si == 0 ||
-               tc::mbar_test_wait(tc::smem_u32(&bars.o_free), (cp.si - 1) & 1));
-          if (ready) {
-            tc::tc_fence_after();
-            const uint32_t pb = sbase + Lay::kOffP + b * kPBytes;
-            const uint32_t vb = sbase + Lay::kOffOp + s * kOpBytes + kOpK;
+      for (int ks = 0; ks < total; ++ks, cs.next()) {
+        const int s = ks % NS;
+        const int b = ks & 1;
+        const int key0 = cs.tile * kN;
+        if (cs.first() && !tc::mbar_wait(&bars.q_full, cs.si & 1, &abort_flag)) break;
+        bool ok;
+        if (TMA && !FP8) {
+          if (key0 < cs.bd.klo || key0 + kN > cs.bd.khi) {
+            ok = tc::mbar_wait(&bars.op_full[s], (edge_parity >> s) & 1, &abort_flag);
+            edge_parity ^= 1u << s;
+          } else {
+            ok = tc::mbar_wait(&bars.tma_full[s], (inner_parity >> s) & 1, &abort_flag);
+            inner_parity ^= 1u << s;
+          }
+        } else {
+          ok = tc::mbar_wait(&bars.op_full[s], (ks / NS) & 1, &abort_flag);
+        }
+        if (!ok) break;
+        if (ks >= 2 && !tc::mbar_wait(&bars.s_empty[b], ((ks >> 1) - 1) & 1, &abort_flag)) break;
+        tc::tc_fence_after();
+        const uint32_t kb = sbase + Lay::kOffOp + s * kOpBytes;
 #pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk) {
-              const uint64_t ad = tc::smem_desc_sw128(pb + kk * 32, 16, 1024);
-              const uint64_t bdsc = tc::smem_desc_sw128(vb + kk * 16 * 128, kBlk, 1024);
-              tc::mma_f16_ss(tmem + kTmemO, ad, bdsc, id_pv, (!first || kk > 0) ? 1u : 0u);
-            }
-            tc::mma_commit(&bars.op_empty[s]);
-            tc::mma_commit(&bars.pv_done[b]);
-            cp.next();
-            ++kp;
-            progressed = true;
-          }
+        for (int kq = 0; kq < kDqk / 16; ++kq) {
+          const uint32_t koff = (kq & 3) * 32;
+          const uint64_t ad = tc::smem_desc_sw128(sbase + (kq >> 2) * kQBlock + koff, 16, 1024);
+          const uint64_t bdsc = tc::smem_desc_sw128(kb + (kq >> 2) * kBlk + koff, 16, 1024);
+          tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, kq > 0 ? 1u : 0u);
         }
-        if (ks < total) {
-          const int s = ks % NS;
-          const int b = ks & 1;
-          const int key0 = cs.tile * kN;
-          const bool edge = !(TMA && !FP8) || key0 < cs.bd.klo || key0 + kN > cs.bd.khi;
-          const bool land = edge ? tc::mbar_test_wait(tc::smem_u32(&bars.op_full[s]),
-                                                     (TMA && !FP8) ? (edge_parity >> s) & 1
-                                                                   : (ks / NS) & 1)
-                                 : tc::mbar_test_wait(tc::smem_u32(&bars.tma_full[s]),
-                                                      (inner_parity >> s) & 1);
-          const bool ready =
-              (!cs.first() || tc::mbar_test_wait(tc::smem_u32(&bars.q_full), cs.si & 1)) &&
-              land &&
-              (ks < 2 ||
-               tc::mbar_test_wait(tc::smem_u32(&bars.s_empty[b]), ((ks >> 1) - 1) & 1));
-          if (ready) {
-            if (TMA && !FP8) {
-              if (edge)
-                edge_parity ^= 1u << s;
-              else
-                inner_parity ^= 1u << s;
-            }
-            tc::tc_fence_after();
-            const uint32_t kb = sbase + Lay::kOffOp + s * kOpBytes;
+        tc::mma_commit(&bars.s_full[b]);
+        if (cs.last()) tc::mma_commit(&bars.q_empty);
+      }
+      tc::mma_commit(&bars.final_done);
+      tc::mbar_wait(&bars.final_done, 0, &abort_flag);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ O += P.V issuer
+    if ((tid & 31) == 0) {
+      const uint32_t id_pv = tc::idesc_f16(kHalf ? 0 : 1, 0, 1, kRows, kDv);
+      Cursor cp;
+      cp.init(a.segs, a.blocks, seg_begin, seg_end);
+      for (int kp = 0; kp < total; ++kp, cp.next()) {
+        const int b = kp & 1;
+        const int s = kp % NS;
+        const bool first = cp.first();
+        if (!tc::mbar_wait(&bars.p_full[b], (kp >> 1) & 1, &abort_flag)) break;
+        // the first P.V of a segment overwrites O: the epilogue of the
+        // previous segment must have read it
+        if (first && cp.si > 0 && !tc::mbar_wait(&bars.o_free, (cp.si - 1) & 1, &abort_flag))
+          break;
+        tc::tc_fence_after();
+        const uint32_t pb = sbase + Lay::kOffP + b * kPBytes;
+        const uint32_t vb = sbase + Lay::kOffOp + s * kOpBytes + kOpK;
 #pragma unroll
-            for (int kq = 0; kq < kDqk / 16; ++kq) {
-              const uint32_t koff = (kq & 3) * 32;
-              const uint64_t ad = tc::smem_desc_sw128(sbase + (kq >> 2) * kQBlock + koff, 16, 1024);
-              const uint64_t bdsc = tc::smem_desc_sw128(kb + (kq >> 2) * kBlk + koff, 16, 1024);
-              tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, kq > 0 ? 1u : 0u);
-            }
-            tc::mma_commit(&bars.s_full[b]);
-            if (cs.last()) tc::mma_commit(&bars.q_empty);
-            cs.next();
-            ++ks;
-            progressed = true;
-          }
+        for (int kk = 0; kk < kN / 16; ++kk) {
+          const uint64_t ad = tc::smem_desc_sw128(pb + kk * 32, 16, 1024);
+          const uint64_t bdsc = tc::smem_desc_sw128(vb + kk * 16 * 128, kBlk, 1024);
+          tc::mma_f16_ss(tmem + kTmemO, ad, bdsc, id_pv, (!first || kk > 0) ? 1u : 0u);
         }
-        if (progressed) {
-          idle_since = 0;
-          idle_polls = 0;
-        } else if ((++idle_polls & 255u) == 0) {
-          // bounded like every other wait: give up after 2 s without progress.
-          // The timer is read only every 256 empty polls: the read is slow
-          // enough to delay the next issue noticeably.
-          if (abort_flag) break;
-          const uint64_t now = tc::globaltimer_ns();
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (now - idle_since > 2000000000ull) {
-            abort_flag = 1;
-            break;
-          }
-        }
+        // P.V of tile k completes after Q.K^T of tile k (P needed S): the
+        // stage's K and V may both be overwritten now
+        tc::mma_commit(&bars.op_empty[s]);
+        tc::mma_commit(&bars.pv_done[b]);
       }
       tc::mma_commit(&bars.final_done);
       tc::mbar_wait(&bars.final_done, 0, &abort_flag);

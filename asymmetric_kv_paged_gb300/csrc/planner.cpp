@@ -50,10 +50,11 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   if ((int64_t)hp.qo_indptr[p->batch] * p->num_q_heads > INT32_MAX / kDqk)
     return ATTN_ERR_UNSUPPORTED;
 
-  hp.threads = 320;
+  hp.threads = 352;
   int64_t max_rows = 0;
   for (int32_t b = 0; b < p->batch; ++b)
     max_rows = std::max<int64_t>(max_rows, (int64_t)(hp.qo_indptr[b + 1] - hp.qo_indptr[b]) * hp.group);
+  // M = 64 halves the Q and P tiles, so one more K/V stage fits.
   hp.block_rows = max_rows <= 64 ? 64 : 128;
   const int32_t rows_per_block = hp.block_rows;
   const int32_t G = hp.group;
@@ -89,17 +90,17 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
     }
   }
 
-  // Deal tiles to CTAs in block order: each CTA takes `target` tiles, cutting
-  // a block where its share ends.  A block remainder of <= `slack` tiles is
-  // kept whole on the current CTA to avoid splits that cost more than they
-  // balance.
+  // Deal tiles to CTAs in block order, cutting a block where a CTA's share
+  // ends.  Each new CTA's share is the remaining tiles over the remaining
+  // CTAs, so rounding never piles up on the last one; a block remainder of at
+  // most `slack` tiles (1/32 of a share) stays on the current CTA rather than
+  // becoming a split of its own.
   const int64_t nb = (int64_t)hp.blocks.size();
   if (nb > 0) {
     const int64_t min_tiles = 2;
-    int64_t target = std::max<int64_t>(min_tiles, (total_tiles + num_sms - 1) / num_sms);
-    const int64_t slack = std::max<int64_t>(1, target / 8);
-    int32_t cta = 0;
-    int64_t room = target;
+    int64_t remaining = total_tiles;
+    int32_t cta = -1;
+    int64_t room = 0, target = 0, slack = 0;
     for (int64_t bi = 0; bi < nb; ++bi) {
       BlockDesc &bd = hp.blocks[bi];
       int32_t t0 = bd.klo / kKeyTile;
@@ -108,14 +109,18 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
       while (t0 < tend) {
         if (room <= 0) {
           ++cta;
+          const int64_t ctas_left = std::max<int64_t>(1, (int64_t)num_sms - cta);
+          target = std::max<int64_t>(min_tiles, (remaining + ctas_left - 1) / ctas_left);
+          slack = target / 32;
           room = target;
         }
-        int64_t left = tend - t0;
-        int64_t take = left <= room + slack ? left : room;
+        const int64_t left = tend - t0;
+        const int64_t take = left <= room + slack ? left : room;
         SegDesc s{(int32_t)bi, t0, (int32_t)(t0 + take), split++};
         hp.segs.push_back(s);
         hp.seg_cta.push_back(cta);
         room -= take;
+        remaining -= take;
         t0 += (int32_t)take;
       }
       bd.num_splits = split;
