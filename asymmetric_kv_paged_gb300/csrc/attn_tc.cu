@@ -59,10 +59,13 @@ template <bool FP8, int MR>
 struct Layout {
   static constexpr int kQBlock = MR * 128;    // one 64-column block of Q
   static constexpr int kQBytes = 3 * kQBlock;
+  // Q is double-buffered where it fits (BF16, M = 64): the next segment's
+  // rows are staged while the current one runs.
+  static constexpr int kQBufs = (!FP8 && MR == 64) ? 2 : 1;
   static constexpr int kPBytes = MR * 128;    // P tile [MR rows x 64 keys]
   static constexpr int kOpStages = FP8 ? (MR == 64 ? 3 : 2) : (MR == 64 ? 4 : 3);
   static constexpr int kRawStages = FP8 ? 3 : 0;
-  static constexpr int kOffOp = kQBytes;
+  static constexpr int kOffOp = kQBufs * kQBytes;
   static constexpr int kOffRaw = kOffOp + kOpStages * kOpBytes;
   static constexpr int kOffP = kOffRaw + kRawStages * kRawBytes;
   static constexpr int kUsed = kOffP + 2 * kPBytes;
@@ -75,7 +78,7 @@ struct Layout {
 struct Bars {
   uint64_t tma_full[4], tma_empty[4], edge_full[4];
   uint64_t op_full[4], op_empty[4];
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t o_free, final_done, sm_sync;
@@ -226,8 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars.op_full[s], 128);
       tc::mbar_init(&bars.op_empty[s], 1);
     }
-    tc::mbar_init(&bars.q_full, 128);
-    tc::mbar_init(&bars.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&bars.q_full[i], 128);
+      tc::mbar_init(&bars.q_empty[i], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&bars.s_full[b], 1);
       tc::mbar_init(&bars.s_empty[b], 128);
@@ -313,7 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < total; ++k, cur.next()) {
       const BlockDesc &bd = cur.bd;
       if (cur.first()) {
-        if (cur.si > 0 && !tc::mbar_wait(&bars.q_empty, (cur.si - 1) & 1, &abort_flag)) break;
+        constexpr int QB = Lay::kQBufs;
+        const int qb = cur.si % QB;
+        if (cur.si >= QB &&
+            !tc::mbar_wait(&bars.q_empty[qb], ((cur.si / QB) - 1) & 1, &abort_flag))
+          break;
+        uint8_t *qs = smem + qb * Lay::kQBytes;
         const int rows_pad = rows_pad_of(bd.nrows);
         for (int idx = ct; idx < kRows * 24; idx += 128) {
           const int p = idx / 24;          // MMA row position
@@ -328,10 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                       ((int64_t)tok * a.hq + h) * kDqk) + ch);
             if (kHalf) v = bf16x8_to_f16x8(v);
           }
-          *reinterpret_cast<uint4 *>(smem + (ch >> 3) * kQBlock + tc::sw128_offset(p, ch & 7)) = v;
+          *reinterpret_cast<uint4 *>(qs + (ch >> 3) * kQBlock + tc::sw128_offset(p, ch & 7)) = v;
         }
         tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&bars.q_full);
+        tc::mbar_arrive(&bars.q_full[qb]);
       }
       const int s = k % NS;
       const int key0 = cur.tile * kN;
@@ -458,7 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = ks % NS;
         const int b = ks & 1;
         const int key0 = cs.tile * kN;
-        if (cs.first() && !tc::mbar_wait(&bars.q_full, cs.si & 1, &abort_flag)) break;
+        constexpr int QB = Lay::kQBufs;
+        const int qb = cs.si % QB;
+        if (cs.first() && !tc::mbar_wait(&bars.q_full[qb], (cs.si / QB) & 1, &abort_flag)) break;
         bool ok;
         if (TMA && !FP8) {
           if (key0 < cs.bd.klo || key0 + kN > cs.bd.khi) {
@@ -478,12 +490,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kq = 0; kq < kDqk / 16; ++kq) {
           const uint32_t koff = (kq & 3) * 32;
-          const uint64_t ad = tc::smem_desc_sw128(sbase + (kq >> 2) * kQBlock + koff, 16, 1024);
+          const uint64_t ad = tc::smem_desc_sw128(sbase + qb * Lay::kQBytes + (kq >> 2) * kQBlock + koff,
+                                                  16, 1024);
           const uint64_t bdsc = tc::smem_desc_sw128(kb + (kq >> 2) * kBlk + koff, 16, 1024);
           tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, kq > 0 ? 1u : 0u);
         }
         tc::mma_commit(&bars.s_full[b]);
-        if (cs.last()) tc::mma_commit(&bars.q_empty);
+        if (cs.last()) tc::mma_commit(&bars.q_empty[qb]);
       }
       tc::mma_commit(&bars.final_done);
       tc::mbar_wait(&bars.final_done, 0, &abort_flag);
@@ -534,6 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_run = 0.f;
     int row_lo = 0, row_hi = 0, rr = 0, rows_pad = kRows, col0 = 0, off = 0, len = kN, nc = kN;
     int zero_pending = 0;
+    int row_tok = 0, row_h = 0;
+    float sink2 = -INFINITY;
     bool valid = false, warp_live = false;
     uint32_t sync_phase = 0;
     // Bounded wait with a warp-uniform outcome: the TMEM loads that follow are
@@ -541,10 +556,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity, &abort_flag));
     };
-    // bounded rendezvous of the 128 softmax threads
+    // bounded rendezvous of the 128 softmax threads; the four warps reach it
+    // together, so it polls instead of sleeping (a suspended wait resumes
+    // well after the phase completes)
     auto group_sync = [&]() -> bool {
       tc::mbar_arrive(&bars.sm_sync);
-      const bool ok = wait(&bars.sm_sync, sync_phase);
+      const bool ok =
+          __all_sync(0xffffffffu, tc::mbar_wait_spin(&bars.sm_sync, sync_phase, &abort_flag));
       sync_phase ^= 1;
       return ok;
     };
@@ -710,7 +728,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         warp_live = __any_sync(0xffffffffu, valid);
         row_lo = row_hi = 0;
+        sink2 = -INFINITY;
         if (valid) {
+          // the row's query token and head, and its sink logit in base 2: read
+          // now, their latency hidden behind the segment's tiles
+          const int flat = bd.row0 + rr;
+          row_tok = bd.tok0 + flat / a.group;
+          row_h = bd.g * a.group + flat % a.group;
+          if (a.sinks) sink2 = a.sinks[row_h] * kLog2e;
           const int i = bd.L - bd.n + (bd.row0 + rr) / a.group;
           row_hi = i + 1;
           row_lo = a.window > 0 ? max(0, i - a.window + 1) : 0;
@@ -743,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           float scale_o = 0.f, lse = -INFINITY;
           if (single) {
-            const float sig = (a.sinks && valid) ? a.sinks[h] * kLog2e : -INFINITY;
+            const float sig = valid ? sink2 : -INFINITY;
             const float MM = fmaxf(m_run, sig);
             if (MM != -INFINITY) {
               const float Z = l_run * exp2f(m_run - MM) + exp2f(sig - MM);
@@ -792,21 +817,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // several copies per row: combine them through shared memory.
-        // sm_m / sm_l: each copy's running max and sum; buf: 32 O columns per
-        // copy at a time, scaled to the row's common max (stride 33: no bank
-        // conflicts); each thread then sums the copies of (row, column) pairs.
+        // Several copies per row (copy c of block row r sits at position
+        // c * rows_pad + r).  Each copy works out the row's common maximum and
+        // normaliser from the copies' statistics, scales its own O row by its
+        // share, and the copies are then summed through shared memory 32
+        // columns at a time (stride 33: no bank conflicts).
         const int copies = kRows / rows_pad;
         if (pos >= 0) {
           sm_m[pos] = valid ? m_run : -INFINITY;
           sm_l[pos] = valid ? l_run : 0.f;
         }
         if (!group_sync()) break;
-        float f = 0.f;
-        if (valid && m_run != -INFINITY) {
+        float f = 0.f, lse = -INFINITY;
+        if (valid) {
           float M = -INFINITY;
           for (int c = 0; c < copies; ++c) M = fmaxf(M, sm_m[c * rows_pad + rr]);
-          f = exp2f(m_run - M);
+          float L = 0.f;
+          if (M != -INFINITY)
+            for (int c = 0; c < copies; ++c) {
+              const float mc = sm_m[c * rows_pad + rr];
+              if (mc != -INFINITY) L += sm_l[c * rows_pad + rr] * exp2f(mc - M);
+            }
+          const float mine = m_run == -INFINITY ? 0.f : 1.f;
+          if (single) {
+            const float MM = fmaxf(M, sink2);
+            if (MM != -INFINITY) {
+              const float Z = L * exp2f(M - MM) + exp2f(sink2 - MM);
+              f = mine * exp2f(m_run - MM) * a.v_scale / Z;
+              lse = (MM + log2f(Z)) * kLn2;
+            }
+          } else if (L > 0.f) {
+            f = mine * exp2f(m_run - M) * a.v_scale / L;
+            lse = M + log2f(L);
+          }
+          if (pos < rows_pad) {          // copy 0 writes the row's log-sum-exp
+            if (single) {
+              if (a.lse_out) a.lse_out[(int64_t)row_tok * a.hq + row_h] = lse;
+            } else {
+              a.part_lse[bd.part_row_base + sd.split * bd.nrows + rr] = lse;
+            }
+          }
         }
         float *buf = reinterpret_cast<float *>(smem + Lay::kOffP);
         const int nout = rows_pad / 4;   // (row, column) outputs per thread per chunk
@@ -819,42 +869,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tmem_wait_ld();
             if (pos >= 0)
 #pragma unroll
-              for (int j = 0; j < 32; ++j) buf[pos * 33 + j] = valid ? f * __uint_as_float(o[j]) : 0.f;
+              for (int j = 0; j < 32; ++j) buf[pos * 33 + j] = f * __uint_as_float(o[j]);
           }
           sync_ok = group_sync() && sync_ok;
 #pragma unroll 1
           for (int i = 0; i < nout; ++i) {
             const int row = (t >> 5) + 4 * i;
             if (!sync_ok || row >= bd.nrows) continue;
-            float v = 0.f, M = -INFINITY, L = 0.f;
-            for (int cp2 = 0; cp2 < copies; ++cp2) {
-              v += buf[(cp2 * rows_pad + row) * 33 + lane];
-              M = fmaxf(M, sm_m[cp2 * rows_pad + row]);
-            }
-            if (M != -INFINITY)
-              for (int cp2 = 0; cp2 < copies; ++cp2) {
-                const float mc = sm_m[cp2 * rows_pad + row];
-                if (mc != -INFINITY) L += sm_l[cp2 * rows_pad + row] * exp2f(mc - M);
-              }
-            const int flat = bd.row0 + row;
-            const int tok = bd.tok0 + flat / a.group;
-            const int h = bd.g * a.group + flat % a.group;
+            float v = 0.f;
+#pragma unroll 4
+            for (int cp2 = 0; cp2 < copies; ++cp2) v += buf[(cp2 * rows_pad + row) * 33 + lane];
             if (single) {
-              const float sig = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
-              const float MM = fmaxf(M, sig);
-              float scale_o = 0.f, lse = -INFINITY;
-              if (MM != -INFINITY) {
-                const float Z = L * exp2f(M - MM) + exp2f(sig - MM);
-                scale_o = exp2f(M - MM) * a.v_scale / Z;
-                lse = (MM + log2f(Z)) * kLn2;
-              }
+              const int flat = bd.row0 + row;
+              const int tok = bd.tok0 + flat / a.group;
+              const int h = bd.g * a.group + flat % a.group;
               static_cast<__nv_bfloat16 *>(a.out)[((int64_t)tok * a.hq + h) * kDv + 32 * c + lane] =
-                  __float2bfloat16_rn(v * scale_o);
-              if (c == 0 && lane == 0 && a.lse_out) a.lse_out[(int64_t)tok * a.hq + h] = lse;
+                  __float2bfloat16_rn(v);
             } else {
               const int prow = bd.part_row_base + sd.split * bd.nrows + row;
-              a.part_o[(int64_t)prow * kDv + 32 * c + lane] = L > 0.f ? v * a.v_scale / L : 0.f;
-              if (c == 0 && lane == 0) a.part_lse[prow] = L > 0.f ? M + log2f(L) : -INFINITY;
+              a.part_o[(int64_t)prow * kDv + 32 * c + lane] = v;
             }
           }
           sync_ok = group_sync() && sync_ok;

@@ -80,6 +80,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// The same wait without sleeping, for short waits on the critical path: a
+// thread woken from a suspended try_wait resumes well after the phase
+// completes.  The time limit is checked every 256 probes.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort,
+                                               uint64_t limit_ns = 2000000000ull) {
+  const uint32_t a = smem_u32(bar);
+  uint64_t t0 = 0;
+#pragma unroll 1
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(a, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > limit_ns) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- fences
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
