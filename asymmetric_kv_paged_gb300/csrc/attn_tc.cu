@@ -214,6 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  // let a programmatic dependent (the split merge) be scheduled now; it
+  // waits for this grid's completion before it reads anything written here
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int seg_begin = a.cta_seg_begin[blockIdx.x];
   const int seg_end = a.cta_seg_begin[blockIdx.x + 1];
   if (seg_begin >= seg_end) return;
