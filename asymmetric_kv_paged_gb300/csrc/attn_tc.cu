@@ -78,6 +78,9 @@ struct Layout {
 struct Bars {
   uint64_t tma_full[4], tma_empty[4], edge_full[4];
   uint64_t op_full[4], op_empty[4];
+  // FP8 + TMA only: V of a stage converted (v_full) and K of a stage read by
+  // the Q.K^T MMAs (k_empty); op_full / op_empty then cover K / V alone
+  uint64_t v_full[4], k_empty[4];
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pv_done[2];
@@ -231,6 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars.edge_full[s], 1);
       tc::mbar_init(&bars.op_full[s], 128);
       tc::mbar_init(&bars.op_empty[s], 1);
+      tc::mbar_init(&bars.v_full[s], 128);
+      tc::mbar_init(&bars.k_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&bars.q_full[i], 128);
@@ -317,35 +322,135 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t *vc = static_cast<const uint8_t *>(a.v_cache);
     Cursor cur;
     cur.init(a.segs, a.blocks, seg_begin, seg_end);
-    uint32_t edge_parity = 0;   // BF16 + TMA: completed edge tiles per stage (one bit each)
-    for (int k = 0; k < total; ++k, cur.next()) {
-      const BlockDesc &bd = cur.bd;
-      if (cur.first()) {
-        constexpr int QB = Lay::kQBufs;
-        const int qb = cur.si % QB;
-        if (cur.si >= QB &&
-            !tc::mbar_wait(&bars.q_empty[qb], ((cur.si / QB) - 1) & 1, &abort_flag))
-          break;
-        uint8_t *qs = smem + qb * Lay::kQBytes;
-        const int rows_pad = rows_pad_of(bd.nrows);
-        for (int idx = ct; idx < kRows * 24; idx += 128) {
+    // Stage the Q rows of the cursor's segment (row position p holds block
+    // row p % rows_pad).  The loads go out 8-12 at a time: under a saturated
+    // K/V stream each round trip to memory takes microseconds.
+    auto stage_q = [&](const Cursor &c) -> bool {
+      constexpr int QB = Lay::kQBufs;
+      const BlockDesc &bd = c.bd;
+      const int qb = c.si % QB;
+      if (c.si >= QB && !tc::mbar_wait_warp(&bars.q_empty[qb], ((c.si / QB) - 1) & 1, &abort_flag))
+        return false;
+      uint8_t *qs = smem + qb * Lay::kQBytes;
+      const int rows_pad = rows_pad_of(bd.nrows);
+      constexpr int kIters = kRows * 24 / 128;
+      constexpr int kBatch = kRows == 128 ? 8 : 12;
+      static_assert(kIters % kBatch == 0, "Q staging batches");
+#pragma unroll 1
+      for (int i0 = 0; i0 < kIters; i0 += kBatch) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int idx = ct + (i0 + u) * 128;
           const int p = idx / 24;          // MMA row position
           const int r = p % rows_pad;      // block row it holds
           const int ch = idx % 24;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          v[u] = make_uint4(0u, 0u, 0u, 0u);
           if (r < bd.nrows) {
             const int flat = bd.row0 + r;
             const int tok = bd.tok0 + flat / a.group;
             const int h = bd.g * a.group + flat % a.group;
-            v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) +
-                                                      ((int64_t)tok * a.hq + h) * kDqk) + ch);
-            if (kHalf) v = bf16x8_to_f16x8(v);
+            v[u] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) +
+                                                         ((int64_t)tok * a.hq + h) * kDqk) + ch);
           }
-          *reinterpret_cast<uint4 *>(qs + (ch >> 3) * kQBlock + tc::sw128_offset(p, ch & 7)) = v;
         }
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&bars.q_full[qb]);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int idx = ct + (i0 + u) * 128;
+          const int p = idx / 24;
+          const int ch = idx % 24;
+          const uint4 w = kHalf ? bf16x8_to_f16x8(v[u]) : v[u];
+          *reinterpret_cast<uint4 *>(qs + (ch >> 3) * kQBlock + tc::sw128_offset(p, ch & 7)) = w;
+        }
       }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars.q_full[qb]);
+      return true;
+    };
+    if constexpr (FP8 && TMA) {
+      // FP8 rows staged by TMA: [64 keys x 192 B] K then [64 keys x 128 B] V.
+      // K of tile k and V of tile k-1 are converted in one step, so V reaches
+      // its operand stage only shortly before P.V needs it and the stage's K
+      // half is handed back as soon as Q.K^T has read it: the two halves of
+      // a stage are released separately (k_empty, op_empty).
+      int pkey0 = 0, pklo = 0, pkhi = 0;   // the previous tile's key range
+      for (int k = 0; k <= total; ++k) {
+        if (k < total) {
+          const BlockDesc &bd = cur.bd;
+          if (cur.first() && !stage_q(cur)) break;
+          const int s = k % NS, t = k % NT;
+          const int key0 = cur.tile * kN;
+          if (k >= NS && !tc::mbar_wait_warp(&bars.k_empty[s], ((k / NS) - 1) & 1, &abort_flag))
+            break;
+          if (!tc::mbar_wait_warp(&bars.tma_full[t], (k / NT) & 1, &abort_flag)) break;
+          const uint8_t *raw = smem + Lay::kOffRaw + t * kRawBytes;
+          uint8_t *dst = smem + Lay::kOffOp + s * kOpBytes;
+          constexpr int kKch = kDqk / 16;            // 16-byte source chunks per K row
+          constexpr int kPer = kN * kKch / 128;
+          uint4 buf[kPer];
+#pragma unroll
+          for (int u = 0; u < kPer; ++u) {
+            const int c = ct + u * 128;
+            buf[u] = *reinterpret_cast<const uint4 *>(raw + (c / kKch) * kDqk + (c % kKch) * 16);
+          }
+#pragma unroll
+          for (int u = 0; u < kPer; ++u) {
+            const int c = ct + u * 128;
+            const int kk = c / kKch, c16 = 2 * (c % kKch);
+            const int j = key0 + kk;
+            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+            if (j >= bd.klo && j < bd.khi) e4m3x16_to_f16(buf[u], lo, hi);
+            *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
+            *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
+                                       tc::sw128_offset(kk, (c16 + 1) & 7)) = hi;
+          }
+          tc::fence_proxy_async_smem();
+          tc::mbar_arrive(&bars.op_full[s]);
+        }
+        if (k >= 1) {
+          const int kv = k - 1;
+          const int s = kv % NS, t = kv % NT;
+          if (kv >= NS && !tc::mbar_wait_warp(&bars.op_empty[s], ((kv / NS) - 1) & 1, &abort_flag))
+            break;
+          const uint8_t *raw = smem + Lay::kOffRaw + t * kRawBytes + kRawK;
+          uint8_t *dst = smem + Lay::kOffOp + s * kOpBytes + kOpK;
+          constexpr int kVch = kDv / 16;
+          constexpr int kPer = kN * kVch / 128;
+          uint4 buf[kPer];
+#pragma unroll
+          for (int u = 0; u < kPer; ++u) {
+            const int c = ct + u * 128;
+            buf[u] = *reinterpret_cast<const uint4 *>(raw + (c / kVch) * kDv + (c % kVch) * 16);
+          }
+#pragma unroll
+          for (int u = 0; u < kPer; ++u) {
+            const int c = ct + u * 128;
+            const int kk = c / kVch, c16 = 2 * (c % kVch);
+            const int j = pkey0 + kk;
+            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+            if (j >= pklo && j < pkhi) e4m3x16_to_f16(buf[u], lo, hi);
+            *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
+            *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
+                                       tc::sw128_offset(kk, (c16 + 1) & 7)) = hi;
+          }
+          // the proxy fence also orders this thread's reads of the raw stage
+          // before the TMA writes that refill it: release it only now
+          tc::fence_proxy_async_smem();
+          tc::mbar_arrive(&bars.v_full[s]);
+          tc::mbar_arrive(&bars.tma_empty[t]);
+        }
+        if (k < total) {
+          pkey0 = cur.tile * kN;
+          pklo = cur.bd.klo;
+          pkhi = cur.bd.khi;
+          cur.next();
+        }
+      }
+    } else {
+    uint32_t edge_parity = 0;   // BF16 + TMA: completed edge tiles per stage (one bit each)
+    for (int k = 0; k < total; ++k, cur.next()) {
+      const BlockDesc &bd = cur.bd;
+      if (cur.first() && !stage_q(cur)) break;
       const int s = k % NS;
       const int key0 = cur.tile * kN;
       uint8_t *op = smem + Lay::kOffOp + s * kOpBytes;
@@ -375,40 +480,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kKch = kDqk * kEs / 16;  // source 16-byte chunks per K row
       constexpr int kVch = kDv * kEs / 16;
       constexpr int kPer = kN * (kKch + kVch) / 128;
-      // chunk u of this thread: (is K, key within the tile, 16-byte chunk of the row)
-      //  TMA staging: consecutive threads take consecutive chunks (conflict-free reads);
-      //  gather: two threads per key, so each thread looks up one page per tile.
+      // Gather (page sizes TMA cannot tile): two threads per key, so each
+      // thread looks up one page per tile.  Chunk u of this thread: (is K,
+      // key within the tile, 16-byte chunk of the row).
       auto chunk_of = [&](int u, bool &is_k, int &kk, int &ch) {
-        if (TMA) {
-          const int c = ct + u * 128;
-          is_k = c < kN * kKch;
-          const int cc = is_k ? c : c - kN * kKch;
-          const int nch = is_k ? kKch : kVch;
-          kk = cc / nch;
-          ch = cc % nch;
-        } else {
-          kk = ct >> 1;
-          const int part = ct & 1;
-          is_k = u < kKch / 2;
-          ch = is_k ? part * (kKch / 2) + u : part * (kVch / 2) + (u - kKch / 2);
-        }
+        kk = ct >> 1;
+        const int part = ct & 1;
+        is_k = u < kKch / 2;
+        ch = is_k ? part * (kKch / 2) + u : part * (kVch / 2) + (u - kKch / 2);
       };
       uint4 buf[kPer];
-      if (TMA) {
-        // FP8 rows staged by TMA: [64 keys x 192 B] K then [64 keys x 128 B] V
-        const int t = k % NT;
-        if (!tc::mbar_wait(&bars.tma_full[t], (k / NT) & 1, &abort_flag)) break;
-        const uint8_t *raw = smem + Lay::kOffRaw + t * kRawBytes;
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          bool is_k;
-          int kk, ch;
-          chunk_of(u, is_k, kk, ch);
-          buf[u] = *reinterpret_cast<const uint4 *>(
-              raw + (is_k ? kk * kDqk + ch * 16 : kRawK + kk * kDv + ch * 16));
-        }
-        tc::mbar_arrive(&bars.tma_empty[t]);
-      } else {
+      {
         // gather: the page of this thread's key, then 16-byte loads of its chunks
         const int j = key0 + (ct >> 1);
         int64_t slot = -1;
@@ -452,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars.op_full[s]);
+    }
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ S = Q.K^T issuer
@@ -499,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, kq > 0 ? 1u : 0u);
         }
         tc::mma_commit(&bars.s_full[b]);
+        if (FP8 && TMA) tc::mma_commit(&bars.k_empty[s]);
         if (cs.last()) tc::mma_commit(&bars.q_empty[qb]);
       }
       tc::mma_commit(&bars.final_done);
@@ -515,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = kp % NS;
         const bool first = cp.first();
         if (!tc::mbar_wait(&bars.p_full[b], (kp >> 1) & 1, &abort_flag)) break;
+        if (FP8 && TMA && !tc::mbar_wait(&bars.v_full[s], (kp / NS) & 1, &abort_flag)) break;
         // the first P.V of a segment overwrites O: the epilogue of the
         // previous segment must have read it
         if (first && cp.si > 0 && !tc::mbar_wait(&bars.o_free, (cp.si - 1) & 1, &abort_flag))
@@ -529,7 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_f16_ss(tmem + kTmemO, ad, bdsc, id_pv, (!first || kk > 0) ? 1u : 0u);
         }
         // P.V of tile k completes after Q.K^T of tile k (P needed S): the
-        // stage's K and V may both be overwritten now
+        // stage's V (and K, where K has no barrier of its own) may be
+        // overwritten now
         tc::mma_commit(&bars.op_empty[s]);
         tc::mma_commit(&bars.pv_done[b]);
       }

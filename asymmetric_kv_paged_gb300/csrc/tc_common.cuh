@@ -80,6 +80,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// The same wait for all 32 lanes of a warp, with a warp-uniform outcome, so
+// that a give-up never splits a warp ahead of a warp-wide operation.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
 // The same wait without sleeping, for short waits on the critical path: a
 // thread woken from a suspended try_wait resumes well after the phase
 // completes.  The time limit is checked every 256 probes.
