@@ -369,82 +369,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if constexpr (FP8 && TMA) {
       // FP8 rows staged by TMA: [64 keys x 192 B] K then [64 keys x 128 B] V.
-      // K of tile k and V of tile k-1 are converted in one step, so V reaches
-      // its operand stage only shortly before P.V needs it and the stage's K
-      // half is handed back as soon as Q.K^T has read it: the two halves of
-      // a stage are released separately (k_empty, op_empty).
-      int pkey0 = 0, pklo = 0, pkhi = 0;   // the previous tile's key range
-      for (int k = 0; k <= total; ++k) {
-        if (k < total) {
-          const BlockDesc &bd = cur.bd;
-          if (cur.first() && !stage_q(cur)) break;
-          const int s = k % NS, t = k % NT;
-          const int key0 = cur.tile * kN;
-          if (k >= NS && !tc::mbar_wait_warp(&bars.k_empty[s], ((k / NS) - 1) & 1, &abort_flag))
-            break;
-          if (!tc::mbar_wait_warp(&bars.tma_full[t], (k / NT) & 1, &abort_flag)) break;
-          const uint8_t *raw = smem + Lay::kOffRaw + t * kRawBytes;
-          uint8_t *dst = smem + Lay::kOffOp + s * kOpBytes;
-          constexpr int kKch = kDqk / 16;            // 16-byte source chunks per K row
-          constexpr int kPer = kN * kKch / 128;
-          uint4 buf[kPer];
+      // Both halves are read into registers and the raw stage goes back to
+      // the TMA producer at once (after a proxy fence: the refill must not
+      // overtake these reads); then K and V are converted into the operand
+      // stage, whose two halves are released separately: K once Q.K^T has
+      // read it (k_empty), V once P.V has (op_empty).
+      for (int k = 0; k < total; ++k, cur.next()) {
+        const BlockDesc &bd = cur.bd;
+        if (cur.first() && !stage_q(cur)) break;
+        const int s = k % NS, t = k % NT;
+        const int key0 = cur.tile * kN;
+        constexpr int kKch = kDqk / 16;            // 16-byte source chunks per K row
+        constexpr int kVch = kDv / 16;
+        constexpr int kPerK = kN * kKch / 128;
+        constexpr int kPerV = kN * kVch / 128;
+        if (!tc::mbar_wait_warp(&bars.tma_full[t], (k / NT) & 1, &abort_flag)) break;
+        const uint8_t *raw = smem + Lay::kOffRaw + t * kRawBytes;
+        uint4 bk[kPerK], bv[kPerV];
 #pragma unroll
-          for (int u = 0; u < kPer; ++u) {
-            const int c = ct + u * 128;
-            buf[u] = *reinterpret_cast<const uint4 *>(raw + (c / kKch) * kDqk + (c % kKch) * 16);
-          }
-#pragma unroll
-          for (int u = 0; u < kPer; ++u) {
-            const int c = ct + u * 128;
-            const int kk = c / kKch, c16 = 2 * (c % kKch);
-            const int j = key0 + kk;
-            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-            if (j >= bd.klo && j < bd.khi) e4m3x16_to_f16(buf[u], lo, hi);
-            *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
-            *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
-                                       tc::sw128_offset(kk, (c16 + 1) & 7)) = hi;
-          }
-          tc::fence_proxy_async_smem();
-          tc::mbar_arrive(&bars.op_full[s]);
+        for (int u = 0; u < kPerK; ++u) {
+          const int c = ct + u * 128;
+          bk[u] = *reinterpret_cast<const uint4 *>(raw + (c / kKch) * kDqk + (c % kKch) * 16);
         }
-        if (k >= 1) {
-          const int kv = k - 1;
-          const int s = kv % NS, t = kv % NT;
-          if (kv >= NS && !tc::mbar_wait_warp(&bars.op_empty[s], ((kv / NS) - 1) & 1, &abort_flag))
-            break;
-          const uint8_t *raw = smem + Lay::kOffRaw + t * kRawBytes + kRawK;
-          uint8_t *dst = smem + Lay::kOffOp + s * kOpBytes + kOpK;
-          constexpr int kVch = kDv / 16;
-          constexpr int kPer = kN * kVch / 128;
-          uint4 buf[kPer];
 #pragma unroll
-          for (int u = 0; u < kPer; ++u) {
-            const int c = ct + u * 128;
-            buf[u] = *reinterpret_cast<const uint4 *>(raw + (c / kVch) * kDv + (c % kVch) * 16);
-          }
+        for (int u = 0; u < kPerV; ++u) {
+          const int c = ct + u * 128;
+          bv[u] = *reinterpret_cast<const uint4 *>(raw + kRawK + (c / kVch) * kDv + (c % kVch) * 16);
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&bars.tma_empty[t]);
+        uint8_t *dst = smem + Lay::kOffOp + s * kOpBytes;
+        if (k >= NS && !tc::mbar_wait_warp(&bars.k_empty[s], ((k / NS) - 1) & 1, &abort_flag))
+          break;
 #pragma unroll
-          for (int u = 0; u < kPer; ++u) {
-            const int c = ct + u * 128;
-            const int kk = c / kVch, c16 = 2 * (c % kVch);
-            const int j = pkey0 + kk;
-            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-            if (j >= pklo && j < pkhi) e4m3x16_to_f16(buf[u], lo, hi);
-            *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
-            *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
-                                       tc::sw128_offset(kk, (c16 + 1) & 7)) = hi;
-          }
-          // the proxy fence also orders this thread's reads of the raw stage
-          // before the TMA writes that refill it: release it only now
-          tc::fence_proxy_async_smem();
-          tc::mbar_arrive(&bars.v_full[s]);
-          tc::mbar_arrive(&bars.tma_empty[t]);
+        for (int u = 0; u < kPerK; ++u) {
+          const int c = ct + u * 128;
+          const int kk = c / kKch, c16 = 2 * (c % kKch);
+          const int j = key0 + kk;
+          uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+          if (j >= bd.klo && j < bd.khi) e4m3x16_to_f16(bk[u], lo, hi);
+          *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
+          *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
+                                     tc::sw128_offset(kk, (c16 + 1) & 7)) = hi;
         }
-        if (k < total) {
-          pkey0 = cur.tile * kN;
-          pklo = cur.bd.klo;
-          pkhi = cur.bd.khi;
-          cur.next();
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&bars.op_full[s]);
+        if (k >= NS && !tc::mbar_wait_warp(&bars.op_empty[s], ((k / NS) - 1) & 1, &abort_flag))
+          break;
+        dst += kOpK;
+#pragma unroll
+        for (int u = 0; u < kPerV; ++u) {
+          const int c = ct + u * 128;
+          const int kk = c / kVch, c16 = 2 * (c % kVch);
+          const int j = key0 + kk;
+          uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+          if (j >= bd.klo && j < bd.khi) e4m3x16_to_f16(bv[u], lo, hi);
+          *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
+          *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
+                                     tc::sw128_offset(kk, (c16 + 1) & 7)) = hi;
         }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&bars.v_full[s]);
       }
     } else {
     uint32_t edge_parity = 0;   // BF16 + TMA: completed edge tiles per stage (one bit each)
