@@ -151,19 +151,18 @@ __device__ __forceinline__ uint32_t cvt_pair(float lo, float hi, bool half) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// 16 E4M3 codes -> 16 fp16 values (exact), as two 16-byte chunks.
+// 16 E4M3 codes -> 16 fp16 values (exact: every E4M3 value is an fp16
+// value), as two 16-byte chunks.  One cvt.rn.f16x2.e4m3x2 turns the two
+// codes of a 16-bit half-word into an fp16 pair, low byte to low half.
 __device__ __forceinline__ void e4m3x16_to_f16(const uint4 raw, uint4 &lo, uint4 &hi) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
   uint32_t h[8];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[q] & 0xFFFFu),
-                                               __NV_E4M3);
-    __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[q] >> 16),
-                                               __NV_E4M3);
-    h[2 * q] = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
-    h[2 * q + 1] = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
-  }
+  for (int q = 0; q < 4; ++q)
+    asm("{\n .reg .b16 l, u;\n mov.b32 {l, u}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n"
+        " cvt.rn.f16x2.e4m3x2 %1, u;\n}\n"
+        : "=r"(h[2 * q]), "=r"(h[2 * q + 1])
+        : "r"(w[q]));
   lo = make_uint4(h[0], h[1], h[2], h[3]);
   hi = make_uint4(h[4], h[5], h[6], h[7]);
 }
