@@ -22,7 +22,7 @@
 //              the K/V boxes (BF16: straight into the 128-byte swizzled
 //              operand layout; FP8: raw rows into a staging ring);
 //   warp 10    issues the O += P.V MMAs (one thread).
-// TMEM: S double buffer (2 x 64 columns) + O (128 columns).
+// TMEM: S double buffer (2 x 64 columns), O (128 columns), P double buffer (2 x 32).
 // Every wait is bounded in time; a broken invariant ends the kernel with bit 1
 // of the plan's error word set instead of hanging the GPU.
 #include <cuda_bf16.h>
@@ -46,8 +46,9 @@ constexpr int kOpK = 3 * kBlk;               // K operand tile: 24 KB
 constexpr int kOpBytes = kOpK + 2 * kBlk;    // + V operand tile: 40 KB
 constexpr int kRawK = kN * kDqk;             // raw E4M3 K rows: 12 KB
 constexpr int kRawBytes = kRawK + kN * kDv;  // + raw V rows: 20 KB
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmemO = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 128;             // O: 128 fp32 columns
+constexpr uint32_t kTmemP = 256;             // P double buffer: 2 x 32 columns (bf16/fp16 pairs)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;    // base-2 growth allowed before O is rescaled
@@ -62,13 +63,14 @@ struct Layout {
   // Q is double-buffered where it fits (BF16, M = 64): the next segment's
   // rows are staged while the current one runs.
   static constexpr int kQBufs = (!FP8 && MR == 64) ? 2 : 1;
-  static constexpr int kPBytes = MR * 128;    // P tile [MR rows x 64 keys]
-  static constexpr int kOpStages = FP8 ? (MR == 64 ? 3 : 2) : (MR == 64 ? 4 : 3);
+  // copy-combine buffer of the epilogue: MR rows x 32 fp32 columns
+  static constexpr int kCombBytes = MR * 32 * 4;
+  static constexpr int kOpStages = FP8 ? (MR == 64 ? 3 : 2) : 4;
   static constexpr int kRawStages = FP8 ? 3 : 0;
   static constexpr int kOffOp = kQBufs * kQBytes;
   static constexpr int kOffRaw = kOffOp + kOpStages * kOpBytes;
-  static constexpr int kOffP = kOffRaw + kRawStages * kRawBytes;
-  static constexpr int kUsed = kOffP + 2 * kPBytes;
+  static constexpr int kOffComb = kOffRaw + kRawStages * kRawBytes;
+  static constexpr int kUsed = kOffComb + kCombBytes;
   static constexpr int kSmem = kUsed + 1024;  // room to align the base to 1024 B
   static constexpr int kTmaStages = FP8 ? kRawStages : kOpStages;
   // 227 KB per CTA, less the 2 KB of static shared memory.
@@ -203,7 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Lay = Layout<FP8, MR>;
   constexpr int kRows = MR;                 // MMA rows (M)
   constexpr int kQBlock = Lay::kQBlock;
-  constexpr int kPBytes = Lay::kPBytes;
   constexpr int NS = Lay::kOpStages;
   constexpr int NT = Lay::kTmaStages;
   constexpr bool kHalf = FP8;  // operand type: fp16 for FP8 caches, bf16 otherwise
@@ -589,13 +590,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (first && cp.si > 0 && !tc::mbar_wait(&bars.o_free, (cp.si - 1) & 1, &abort_flag))
           break;
         tc::tc_fence_after();
-        const uint32_t pb = sbase + Lay::kOffP + b * kPBytes;
         const uint32_t vb = sbase + Lay::kOffOp + s * kOpBytes + kOpK;
 #pragma unroll
         for (int kk = 0; kk < kN / 16; ++kk) {
-          const uint64_t ad = tc::smem_desc_sw128(pb + kk * 32, 16, 1024);
           const uint64_t bdsc = tc::smem_desc_sw128(vb + kk * 16 * 128, kBlk, 1024);
-          tc::mma_f16_ss(tmem + kTmemO, ad, bdsc, id_pv, (!first || kk > 0) ? 1u : 0u);
+          tc::mma_f16_ts(tmem + kTmemO, tmem + kTmemP + b * 32 + kk * 8, bdsc, id_pv,
+                         (!first || kk > 0) ? 1u : 0u);
         }
         // P.V of tile k completes after Q.K^T of tile k (P needed S): the
         // stage's V (and K, where K has no barrier of its own) may be
@@ -697,17 +697,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (want_max) m_run = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
       }
-      uint8_t *prow = smem + Lay::kOffP + b * kPBytes;
-      const int ch0 = col0 >> 3;
+      // P of this thread's row: 16-bit pairs in TMEM columns kTmemP + 32b + key/2
+      const uint32_t pcol = tmem + lane_base + kTmemP + b * 32;
+      const int g0 = col0 >> 4;          // first 16-key group of the window
       if (zero_pending > 0) {
         // P columns outside the window stay zero for the whole segment: write
         // them once per buffer (the first two tiles), not on every tile
         --zero_pending;
-        if (pos >= 0)
+        const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll 1
-          for (int ch = 0; ch < 8; ++ch)
-            if (ch < ch0 || ch >= ch0 + 2 * nch)
-              *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch)) = make_uint4(0u, 0u, 0u, 0u);
+        for (int gi = 0; gi < kN / 16; ++gi)
+          if (gi < g0 || gi >= g0 + nch) tc::tmem_st8(pcol + 8 * gi, z);
       }
       // exp pass over chunk c held in raw: P = 2^(s * sc - m) to smem, row sums
       // and the raw maximum
@@ -724,12 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           rs[(j >> 1) & 3] += p0 + p1;
           pk[j / 2] = cvt_pair(p0, p1, kHalf);
         }
-        if (pos >= 0) {
-          *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch0 + 2 * c)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(pos, ch0 + 2 * c + 1)) =
-              make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
+        tc::tmem_st8(pcol + 8 * (g0 + c), pk);
       };
 #pragma unroll 1
       for (int pass = 0;; ++pass) {
@@ -773,10 +768,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run *= alpha;
         if (need) m_run = m_tile;
       }
+      tc::tmem_wait_st();                // P is in TMEM before p_full is signalled
       tc::tc_fence_before();
       tc::mbar_arrive(&bars.s_empty[b]);
       l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      tc::fence_proxy_async_smem();
       return true;
     };
 
@@ -894,7 +889,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // c * rows_pad + r).  Each copy works out the row's common maximum and
         // normaliser from the copies' statistics, scales its own O row by its
         // share, and the copies are then summed through shared memory 32
-        // columns at a time (stride 33: no bank conflicts).
+        // columns at a time (rows of 32 floats, XOR-swizzled by row: no bank
+        // conflicts).
         const int copies = kRows / rows_pad;
         if (pos >= 0) {
           sm_m[pos] = valid ? m_run : -INFINITY;
@@ -931,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        float *buf = reinterpret_cast<float *>(smem + Lay::kOffP);
+        float *buf = reinterpret_cast<float *>(smem + Lay::kOffComb);
         const int nout = rows_pad / 4;   // (row, column) outputs per thread per chunk
         bool sync_ok = true;
 #pragma unroll 1
@@ -942,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tmem_wait_ld();
             if (pos >= 0)
 #pragma unroll
-              for (int j = 0; j < 32; ++j) buf[pos * 33 + j] = f * __uint_as_float(o[j]);
+              for (int j = 0; j < 32; ++j) buf[pos * 32 + (j ^ (pos & 31))] = f * __uint_as_float(o[j]);
           }
           sync_ok = group_sync() && sync_ok;
 #pragma unroll 1
@@ -951,7 +947,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!sync_ok || row >= bd.nrows) continue;
             float v = 0.f;
 #pragma unroll 4
-            for (int cp2 = 0; cp2 < copies; ++cp2) v += buf[(cp2 * rows_pad + row) * 33 + lane];
+            for (int cp2 = 0; cp2 < copies; ++cp2) {
+              const int p2 = cp2 * rows_pad + row;
+              v += buf[p2 * 32 + (lane ^ (p2 & 31))];
+            }
             if (single) {
               const int flat = bd.row0 + row;
               const int tok = bd.tok0 + flat / a.group;

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&bar, 1);
     tc::fence_mbar_init();
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, 128);
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 512);
 
   if (mode == 0) {
     stage_sw128(sa, a, 128, 192);   // [128 x 192] K-major
@@ -55,15 +55,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (mode == 2) {
     stage_sw128(sa, a, 64, 192);    // [64 x 192] K-major
     stage_sw128(sb, b, 64, 192);    // [64 x 192] K-major
-  } else {
+  } else if (mode == 1) {
     stage_sw128(sa, a, 128, 64);    // [128 x 64] K-major
     stage_sw128(sb, b, 64, 128);    // [64 keys x 128] stored key-major: MN-major B
+  } else {
+    stage_sw128(sb, b, 64, 128);    // modes 3/4: only V in shared memory
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  const int M = (mode == 2 || mode == 4) ? 64 : 128;
+  if (mode >= 3) {
+    // A = P [M x 64] into TMEM columns 256..287, each thread its own row's
+    // lane (M = 64: rows 16w..16w+15 in lanes 0-15 of warp w's quadrant)
+    const int lane = threadIdx.x & 31;
+    const int row = M == 128 ? (int)threadIdx.x : (lane < 16 ? warp * 16 + lane : -1);
+    uint32_t r[32];
+    for (int j = 0; j < 32; ++j)
+      r[j] = row >= 0 ? *reinterpret_cast<const uint32_t *>(a + (size_t)row * 64 + 2 * j) : 0u;
+    tc::tmem_st32(tmem + ((uint32_t)(warp * 32) << 16) + 256, r);
+    tc::tmem_wait_st();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+  }
 
   if (threadIdx.x == 0) {
     const uint32_t a0 = tc::smem_u32(sa);
@@ -84,6 +101,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd = tc::smem_desc_sw128(b0 + (ks / 4) * 64 * 128 + koff, 16, 1024);
         tc::mma_f16_ss(tmem, ad, bd, idesc, ks > 0);
       }
+    } else if (mode >= 3) {
+      const uint32_t idesc = tc::idesc_f16(ab_type, 0, 1, M, 128);
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bd = tc::smem_desc_sw128(b0 + kk * 16 * 128, 64 * 128, 1024);
+        tc::mma_f16_ts(tmem, tmem + 256 + kk * 8, bd, idesc, kk > 0);
+      }
     } else {
       const uint32_t idesc = tc::idesc_f16(ab_type, 0, 1, 128, 128);
       const uint32_t lbo = variant == 0 ? 64 * 128 : 1024;   // between 64-wide N blocks
@@ -99,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool ok = tc::mbar_wait(&bar, 0, &abort_flag);
   tc::tc_fence_after();
   const int ncols = mode == 0 ? n : (mode == 2 ? 64 : 128);
+  (void)M;
   if (ok) {
     const int row = threadIdx.x;   // TMEM lane = row; warp w owns lanes 32w..32w+31
     for (int c0 = 0; c0 < ncols; c0 += 32) {
@@ -112,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -121,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 extern "C" attn_status_t attn_debug_tc_gemm(int32_t mode, int32_t variant, int32_t ab_type,
                                             int32_t n, const void *a, const void *b, float *d,
                                             int32_t *status, void *stream) {
-  if (mode < 0 || mode > 2) return ATTN_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 4) return ATTN_ERR_INVALID_ARG;
   if (mode == 0 && n != 64 && n != 128) return ATTN_ERR_INVALID_ARG;
   if (variant != 0 && variant != 1) return ATTN_ERR_INVALID_ARG;
   if (ab_type != 0 && ab_type != 1) return ATTN_ERR_INVALID_ARG;

@@ -25,7 +25,13 @@ extern "C" {
  *           of b (0: leading offset, 1: stride offset);
  *   mode 2: the M=64 form: a[64 x 192] * b[64 x 192]^T; d receives all 128
  *           TMEM lanes x 64 columns as d[128 x 64], so the test can check
- *           which lanes hold the 64 rows (unused lanes hold whatever TMEM had).
+ *           which lanes hold the 64 rows (unused lanes hold whatever TMEM had);
+ *   mode 3: d[128 x 128] = a[128 x 64] * b[64 x 128] with a read from tensor
+ *           memory (row r written by thread r into its lane, two elements per
+ *           32-bit column, element 2j in the low half), b MN-major as in
+ *           mode 1 variant 0 (the P.V form with P kept in TMEM);
+ *   mode 4: mode 3 with M = 64: a[64 x 64], row r written into lane
+ *           32*(r/16) + r%16; d receives all 128 lanes x 128 columns.
  * a, b: device 16-bit matrices, row-major (ab_type 0 = fp16, 1 = bf16);
  * d: device fp32, row-major; status: device int32, set to 1 if the
  * completion wait timed out (left untouched otherwise).  Asynchronous on

@@ -69,3 +69,24 @@ def test_m64_accumulator_lanes():
                 found[r] = lane
     expect = {r: 32 * (r // 16) + r % 16 for r in range(64)}
     assert found == expect, f"row -> lane map: {sorted(found.items())}"
+
+
+@pytest.mark.parametrize("mode,rows", [(3, 128), (4, 64)])
+def test_pv_with_p_in_tmem(mode, rows):
+    """P.V with the A operand (P) read from tensor memory: each row written by
+    the thread that owns its accumulator lane, two bf16 values per column."""
+    import numpy as np
+    g = torch.Generator(device="cuda").manual_seed(5 + mode)
+    a = torch.rand(rows, 64, device="cuda", generator=g).to(torch.bfloat16)
+    b = torch.randn(64, 128, device="cuda", generator=g).to(torch.bfloat16)
+    from asymmetric_kv_paged_gb300 import binding as B
+    d = torch.zeros((128, 128), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.attn_debug_tc_gemm(mode, 0, 1, 64, a, b, d, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = (a.float() @ b.float()).cpu().numpy()
+    got = d.cpu().numpy()
+    lanes = [r if rows == 128 else 32 * (r // 16) + r % 16 for r in range(rows)]
+    err = np.abs(got[lanes] - ref).max()
+    assert err < 1e-3 * np.abs(ref).max(), f"max err {err:.3g}"
