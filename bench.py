@@ -339,14 +339,16 @@ def measure_extra(name: str, pk: dict, steps: int, warmup: int, world: int):
         out = {"workload": name, "value": flops / (r["attn_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": r["attn_ms"], "roofline": {"bound": "tensor", "achieved": achieved,
                                                            "peak": peak, "unit": "TFLOP/s",
-                                                           "frac": achieved / peak}}
+                                                           "frac": achieved / peak,
+                                                           "traffic": split_kernel_traffic(name)}}
     else:
         achieved = nbytes / (r["split_ms"] * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
         out = {"workload": name, "value": nbytes / (r["attn_ms"] * 1e-3) / 1e9, "unit": "GB/s",
                "ms_per_step": r["attn_ms"], "roofline": {"bound": "hbm", "achieved": achieved,
                                                            "peak": peak, "unit": "GB/s",
-                                                           "frac": achieved / peak}}
+                                                           "frac": achieved / peak,
+                                                           "traffic": split_kernel_traffic(name)}}
     out.update(split_ms=r["split_ms"], merge_ms=r["merge_ms"], algorithmic_bytes=nbytes,
                flops=flops, l2="flushed between steps" if small else "inputs larger than L2")
     del dw
