@@ -54,9 +54,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;    // base-2 growth allowed before O is rescaled
 
 // Shared-memory layout for MR MMA rows (64 or 128): Q as three 64-column
-// blocks of MR rows, the K/V operand ring, the FP8 staging ring, and two P
-// tiles.  The smaller Q and P of MR = 64 leave room for one more K/V stage.
-template <bool FP8, int MR>
+// blocks of MR rows (two buffers where they fit), the K/V operand ring, the
+// FP8 staging ring and the epilogue's copy-combine buffer.  P lives in TMEM.
+template <bool FP8, int MR, bool TMA>
 struct Layout {
   static constexpr int kQBlock = MR * 128;    // one 64-column block of Q
   static constexpr int kQBytes = 3 * kQBlock;
@@ -65,12 +65,16 @@ struct Layout {
   static constexpr int kQBufs = (!FP8 && MR == 64) ? 2 : 1;
   // copy-combine buffer of the epilogue: MR rows x 32 fp32 columns
   static constexpr int kCombBytes = MR * 32 * 4;
-  static constexpr int kOpStages = FP8 ? (MR == 64 ? 3 : 2) : 4;
+  static constexpr int kOpStages = FP8 ? (MR == 64 ? 3 : 2) : (TMA || MR == 64 ? 4 : 3);
   static constexpr int kRawStages = FP8 ? 3 : 0;
   static constexpr int kOffOp = kQBufs * kQBytes;
   static constexpr int kOffRaw = kOffOp + kOpStages * kOpBytes;
   static constexpr int kOffComb = kOffRaw + kRawStages * kRawBytes;
-  static constexpr int kUsed = kOffComb + kCombBytes;
+  // gather mode: a ring of kSlotRing tiles of resolved cache slots (one int64
+  // per key, -1 for none), filled ahead by the producer warp
+  static constexpr int kSlotRing = TMA ? 0 : 8;
+  static constexpr int kOffSlots = kOffComb + kCombBytes;
+  static constexpr int kUsed = kOffSlots + kSlotRing * kN * 8;
   static constexpr int kSmem = kUsed + 1024;  // room to align the base to 1024 B
   static constexpr int kTmaStages = FP8 ? kRawStages : kOpStages;
   // 227 KB per CTA, less the 2 KB of static shared memory.
@@ -87,6 +91,7 @@ struct Bars {
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t o_free, final_done, sm_sync;
+  uint64_t slot_full[8], slot_empty[8];   // gather mode: the slot ring
 };
 
 // Walks the CTA's tiles in order: segment, tile id, first/last flags.  The
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // and a reference into kernel-parameter space would turn every field read
   // inside them into a memory load that the K/V stream keeps evicting.
   const RunArgs a = args;
-  using Lay = Layout<FP8, MR>;
+  using Lay = Layout<FP8, MR, TMA>;
   constexpr int kRows = MR;                 // MMA rows (M)
   constexpr int kQBlock = Lay::kQBlock;
   constexpr int NS = Lay::kOpStages;
@@ -250,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&bars.o_free, 128);
     tc::mbar_init(&bars.final_done, 2);
     tc::mbar_init(&bars.sm_sync, 128);
+    for (int r = 0; r < 8; ++r) {
+      tc::mbar_init(&bars.slot_full[r], 32);
+      tc::mbar_init(&bars.slot_empty[r], 128);
+    }
     tc::fence_mbar_init();
   }
   if (warp == 8) tc::tmem_alloc(&tmem_slot, kTmemCols);
@@ -261,6 +270,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
+    if (!TMA) {
+      // Gather mode: the warp resolves every key's cache slot (page lookup)
+      // and fills the slot ring up to kSlotRing tiles ahead of the converters,
+      // four tiles per round trip to memory: each lane looks up two keys of
+      // each of the four tiles before storing any of them.
+      constexpr int R = Lay::kSlotRing;
+      constexpr int kBatchTiles = 4;
+      const int ln = tid & 31;
+      int64_t *ring = reinterpret_cast<int64_t *>(smem + Lay::kOffSlots);
+      Cursor cur;
+      cur.init(a.segs, a.blocks, seg_begin, seg_end);
+      bool ok = true;
+      for (int k0 = 0; k0 < total && ok; k0 += kBatchTiles) {
+        int64_t sl[kBatchTiles][2];
+#pragma unroll
+        for (int u = 0; u < kBatchTiles; ++u) {
+          const BlockDesc &bd = cur.bd;
+          const int32_t *pt_row = a.page_table + (int64_t)bd.b * a.pt_stride;
+          const int key0 = cur.tile * kN;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int j = key0 + 2 * ln + q;
+            sl[u][q] = -1;
+            if (k0 + u < total && j >= bd.klo && j < bd.khi) {
+              const int32_t page = __ldg(pt_row + j / a.page_size);
+              if (page >= 0 && page < a.num_pages)
+                sl[u][q] = (int64_t)page * a.page_size + j % a.page_size;
+              else
+                atomicOr(a.err, 1);
+            }
+          }
+          if (k0 + u < total) cur.next();
+        }
+#pragma unroll
+        for (int u = 0; u < kBatchTiles; ++u) {
+          const int k = k0 + u;
+          if (k >= total) break;
+          const int r = k % R;
+          if (k >= R && !tc::mbar_wait_warp(&bars.slot_empty[r], ((k / R) - 1) & 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          ring[r * kN + 2 * ln] = sl[u][0];
+          ring[r * kN + 2 * ln + 1] = sl[u][1];
+          tc::mbar_arrive(&bars.slot_full[r]);
+        }
+      }
+    }
     if (TMA && (tid & 31) == 0) {
       const int box = a.page_size >= kN ? kN : a.page_size;   // key rows per box
       const int nbox = kN / box;
@@ -460,14 +517,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(&bars.op_full[s]);
         continue;
       }
-      if (k >= NS && !tc::mbar_wait(&bars.op_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
       constexpr int kEs = FP8 ? 1 : 2;
       constexpr int kKch = kDqk * kEs / 16;  // source 16-byte chunks per K row
       constexpr int kVch = kDv * kEs / 16;
       constexpr int kPer = kN * (kKch + kVch) / 128;
-      // Gather (page sizes TMA cannot tile): two threads per key, so each
-      // thread looks up one page per tile.  Chunk u of this thread: (is K,
-      // key within the tile, 16-byte chunk of the row).
+      // Gather (page sizes TMA cannot tile): two threads per key.  The key's
+      // cache slot comes from the ring the producer warp fills ahead; the row
+      // loads go out before the wait for a free operand stage, so their
+      // latency overlaps it.  Chunk u of this thread: (is K, key within the
+      // tile, 16-byte chunk of the row).
       auto chunk_of = [&](int u, bool &is_k, int &kk, int &ch) {
         kk = ct >> 1;
         const int part = ct & 1;
@@ -476,16 +534,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       uint4 buf[kPer];
       {
-        // gather: the page of this thread's key, then 16-byte loads of its chunks
-        const int j = key0 + (ct >> 1);
-        int64_t slot = -1;
-        if (j >= bd.klo && j < bd.khi) {
-          const int32_t page = __ldg(a.page_table + (int64_t)bd.b * a.pt_stride + j / a.page_size);
-          if (page >= 0 && page < a.num_pages)
-            slot = (int64_t)page * a.page_size + j % a.page_size;
-          else
-            atomicOr(a.err, 1);
-        }
+        constexpr int R = Lay::kSlotRing;
+        const int r = k % R;
+        if (!tc::mbar_wait_warp(&bars.slot_full[r], (k / R) & 1, &abort_flag)) break;
+        const int64_t slot = reinterpret_cast<const int64_t *>(smem + Lay::kOffSlots)[r * kN + (ct >> 1)];
+        tc::mbar_arrive(&bars.slot_empty[r]);
         const int64_t srow = (slot >= 0 ? slot : 0) * a.hkv + bd.g;
         const uint4 *krow = reinterpret_cast<const uint4 *>(kc + srow * (kDqk * kEs));
         const uint4 *vrow = reinterpret_cast<const uint4 *>(vc + srow * (kDv * kEs));
@@ -497,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           buf[u] = slot >= 0 ? __ldg((is_k ? krow : vrow) + ch) : make_uint4(0u, 0u, 0u, 0u);
         }
       }
+      if (k >= NS && !tc::mbar_wait(&bars.op_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         bool is_k;
@@ -981,14 +1035,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool FP8, bool TMA, int MR>
 cudaError_t launch_one(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
-  attn_tc_kernel<FP8, TMA, MR><<<hp.num_ctas, kThreads, Layout<FP8, MR>::kSmem, st>>>(a, m);
+  attn_tc_kernel<FP8, TMA, MR><<<hp.num_ctas, kThreads, Layout<FP8, MR, TMA>::kSmem, st>>>(a, m);
   return cudaGetLastError();
 }
 
 template <bool FP8, bool TMA, int MR>
 cudaError_t prepare_one() {
   return cudaFuncSetAttribute(attn_tc_kernel<FP8, TMA, MR>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<FP8, MR>::kSmem);
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<FP8, MR, TMA>::kSmem);
 }
 
 template <int MR>
