@@ -98,6 +98,7 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   // most `slack` tiles (1/32 of a share) stays on the current CTA rather than
   // becoming a split of its own.
   const int64_t nb = (int64_t)hp.blocks.size();
+  constexpr int64_t kWholeBlockTiles = 8;
   if (nb > 0) {
     const int64_t min_tiles = 2;
     int64_t remaining = total_tiles;
@@ -117,7 +118,18 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
           room = target;
         }
         const int64_t left = tend - t0;
-        const int64_t take = left <= room + slack ? left : room;
+        // A small block (at most kWholeBlockTiles, and at most two shares) is
+        // not split while there are CTAs enough for every block still to
+        // place: a fresh CTA takes it whole, a CTA it does not fit in leaves it
+        // to the next one.  For such a block a split's extra segment and merge
+        // cost more than the room left unused.
+        const bool whole = t0 == bd.klo / kKeyTile && left <= kWholeBlockTiles &&
+                           left <= 2 * target && nb - bi <= (int64_t)num_sms - cta - 1;
+        if (whole && room < target && left > room + slack) {
+          room = 0;
+          continue;
+        }
+        const int64_t take = (whole || left <= room + slack) ? left : room;
         SegDesc s{(int32_t)bi, t0, (int32_t)(t0 + take), split++};
         hp.segs.push_back(s);
         hp.seg_cta.push_back(cta);
