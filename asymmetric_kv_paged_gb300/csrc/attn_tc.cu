@@ -53,6 +53,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;    // base-2 growth allowed before O is rescaled
 
+// Gather mode only: the barriers of the slot ring, kept in dynamic shared
+// memory behind the ring so the TMA kernels' static layout is unchanged.
+struct SlotBars {
+  uint64_t full[8], empty[8];
+};
+
 // Shared-memory layout for MR MMA rows (64 or 128): Q as three 64-column
 // blocks of MR rows (two buffers where they fit), the K/V operand ring, the
 // FP8 staging ring and the epilogue's copy-combine buffer.  P lives in TMEM.
@@ -74,7 +80,8 @@ struct Layout {
   // per key, -1 for none), filled ahead by the producer warp
   static constexpr int kSlotRing = TMA ? 0 : 8;
   static constexpr int kOffSlots = kOffComb + kCombBytes;
-  static constexpr int kUsed = kOffSlots + kSlotRing * kN * 8;
+  static constexpr int kOffSlotBars = kOffSlots + kSlotRing * kN * 8;
+  static constexpr int kUsed = kOffSlotBars + (TMA ? 0 : (int)sizeof(SlotBars));
   static constexpr int kSmem = kUsed + 1024;  // room to align the base to 1024 B
   static constexpr int kTmaStages = FP8 ? kRawStages : kOpStages;
   // 227 KB per CTA, less the 2 KB of static shared memory.
@@ -91,8 +98,8 @@ struct Bars {
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t o_free, final_done, sm_sync;
-  uint64_t slot_full[8], slot_empty[8];   // gather mode: the slot ring
 };
+
 
 // Walks the CTA's tiles in order: segment, tile id, first/last flags.  The
 // current segment and its block are cached in registers, so a tile step reads
@@ -255,9 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&bars.o_free, 128);
     tc::mbar_init(&bars.final_done, 2);
     tc::mbar_init(&bars.sm_sync, 128);
-    for (int r = 0; r < 8; ++r) {
-      tc::mbar_init(&bars.slot_full[r], 32);
-      tc::mbar_init(&bars.slot_empty[r], 128);
+    if (!TMA) {
+      SlotBars *sb = reinterpret_cast<SlotBars *>(smem + Lay::kOffSlotBars);
+      for (int r = 0; r < 8; ++r) {
+        tc::mbar_init(&sb->full[r], 32);
+        tc::mbar_init(&sb->empty[r], 128);
+      }
     }
     tc::fence_mbar_init();
   }
@@ -267,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const uint32_t sbase = tc::smem_u32(smem);
+  SlotBars *slot_bars = reinterpret_cast<SlotBars *>(smem + Lay::kOffSlotBars);
 
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
@@ -308,13 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int k = k0 + u;
           if (k >= total) break;
           const int r = k % R;
-          if (k >= R && !tc::mbar_wait_warp(&bars.slot_empty[r], ((k / R) - 1) & 1, &abort_flag)) {
+          if (k >= R && !tc::mbar_wait_warp(&slot_bars->empty[r], ((k / R) - 1) & 1, &abort_flag)) {
             ok = false;
             break;
           }
           ring[r * kN + 2 * ln] = sl[u][0];
           ring[r * kN + 2 * ln + 1] = sl[u][1];
-          tc::mbar_arrive(&bars.slot_full[r]);
+          tc::mbar_arrive(&slot_bars->full[r]);
         }
       }
     }
@@ -536,9 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         constexpr int R = Lay::kSlotRing;
         const int r = k % R;
-        if (!tc::mbar_wait_warp(&bars.slot_full[r], (k / R) & 1, &abort_flag)) break;
+        if (!tc::mbar_wait_warp(&slot_bars->full[r], (k / R) & 1, &abort_flag)) break;
         const int64_t slot = reinterpret_cast<const int64_t *>(smem + Lay::kOffSlots)[r * kN + (ct >> 1)];
-        tc::mbar_arrive(&bars.slot_empty[r]);
+        tc::mbar_arrive(&slot_bars->empty[r]);
         const int64_t srow = (slot >= 0 ? slot : 0) * a.hkv + bd.g;
         const uint4 *krow = reinterpret_cast<const uint4 *>(kc + srow * (kDqk * kEs));
         const uint4 *vrow = reinterpret_cast<const uint4 *>(vc + srow * (kDv * kEs));
