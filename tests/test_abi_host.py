@@ -143,3 +143,22 @@ def test_named_configs_schedule_shape():
         info = B.attn_plan_info(plan)
         assert info["rows_per_block"] == rows, name
         assert 0 < info["ctas"] <= 152
+
+
+def test_small_blocks_are_not_split_when_ctas_suffice():
+    # 64 requests of a windowed mix (2-3 key tiles per block, 128 blocks) on 152
+    # SMs: every block fits a CTA of its own, so none is cut and no merge runs
+    seq = [8192] * 64
+    n = [1, 8] * 32
+    prob, keep = B.make_problem(batch=64, num_q_heads=16, num_kv_heads=2, page_size=128,
+                                num_pages=9375, page_table_stride=64, kv_dtype=0, window=128,
+                                has_sinks=False, qo_indptr=np.concatenate([[0], np.cumsum(n)]),
+                                seq_lens=seq)
+    plan = B.attn_plan_host(prob, 152, keep)
+    info = B.attn_plan_info(plan)
+    assert info["multi_split_blocks"] == 0 and info["workspace_bytes"] == 0
+    assert info["segments"] == info["blocks"] == 128
+    # with fewer SMs than blocks the same blocks are dealt (and cut) as usual
+    plan = B.attn_plan_host(prob, 100, keep)
+    info = B.attn_plan_info(plan)
+    assert info["ctas"] <= 100 and info["segments"] >= info["blocks"]
