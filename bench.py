@@ -392,13 +392,7 @@ def run_ours(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64; bf16 N(0,1) values, K scaled 0.5)",
-        "config": {"workload": args.workload, "batch": w.batch, "q_tokens_per_request": 1,
-                   "num_q_heads": w.hq, "num_kv_heads": w.hkv, "head_dim_qk": DQK,
-                   "head_dim_v": DV, "page_size": w.page_size, "pool_slots": w.num_pages * w.page_size,
-                   "kv_tokens": int(w.seq_lens.sum()), "kv_dtype": w.kv_dtype,
-                   "algorithmic_bytes_per_step": nbytes,
-                   "l2": "inputs larger than L2 (KV stream per step >> 129 MB); no flush",
-                   "parallelism": f"replicas x{world} (independent requests, no collective)"},
+        "config": workload_config(w, nbytes, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": split_kernel_traffic(args.workload),
                      "kernel": "attn_tc_kernel", "kernel_ms": split_ms, "merge_ms": r["merge_ms"],
@@ -426,6 +420,18 @@ def run_ours(args):
 
 
 # ---------------------------------------------------------------- reference arm
+
+def workload_config(w, nbytes: int, world: int) -> dict:
+    """The `config` object of the JSON line; both arms report the same one."""
+    return {"workload": w.name, "batch": w.batch,
+            "q_tokens_per_request": int(w.qo_indptr[1] - w.qo_indptr[0]) if w.batch else 0,
+            "num_q_heads": w.hq, "num_kv_heads": w.hkv, "head_dim_qk": DQK, "head_dim_v": DV,
+            "page_size": w.page_size, "pool_slots": w.num_pages * w.page_size,
+            "kv_tokens": int(w.seq_lens.sum()), "kv_dtype": w.kv_dtype,
+            "algorithmic_bytes_per_step": nbytes,
+            "l2": "inputs larger than L2 (KV stream per step >> 129 MB); no flush",
+            "parallelism": f"replicas x{world} (independent requests, no collective)"}
+
 
 def run_reference(args):
     """The FP64 oracle as it stands, on the host cores: each step computes a bounded
@@ -456,7 +462,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy PCG64)",
-            "config": {"workload": args.workload, "parallelism": "host cores (OpenMP)"},
+            "config": workload_config(w, algorithmic_bytes(w), world),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
