@@ -31,7 +31,14 @@ extern "C" {
  *           32-bit column, element 2j in the low half), b MN-major as in
  *           mode 1 variant 0 (the P.V form with P kept in TMEM);
  *   mode 4: mode 3 with M = 64: a[64 x 64], row r written into lane
- *           32*(r/16) + r%16; d receives all 128 lanes x 128 columns.
+ *           32*(r/16) + r%16; d receives all 128 lanes x 128 columns;
+ *   mode 5: the product of mode 2, then read back with the 16-lane shapes:
+ *           d[0 : 4096] = each thread's 32 registers of a 16x256b.x8 load
+ *           (index (warp*32 + thread)*32 + register); then every thread
+ *           stores the values warp*100000 + thread*100 + j (j < 16) with a
+ *           16x128b.x8 store at column 64, and d[4096 : 6144] receives a
+ *           32x32b load of those 16 columns (index (warp*32 + lane)*16 + col)
+ *           as floats.  d must hold 6144 floats.
  * a, b: device 16-bit matrices, row-major (ab_type 0 = fp16, 1 = bf16);
  * d: device fp32, row-major; status: device int32, set to 1 if the
  * completion wait timed out (left untouched otherwise).  Asynchronous on

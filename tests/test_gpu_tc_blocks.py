@@ -90,3 +90,39 @@ def test_pv_with_p_in_tmem(mode, rows):
     lanes = [r if rows == 128 else 32 * (r // 16) + r % 16 for r in range(rows)]
     err = np.abs(got[lanes] - ref).max()
     assert err < 1e-3 * np.abs(ref).max(), f"max err {err:.3g}"
+
+
+def test_sixteen_lane_tmem_shapes():
+    """The 16x256b / 16x128b TMEM access shapes on an M=64 accumulator: thread
+    t of warp w sees rows 16w + t/4 and 16w + t/4 + 8, column pairs
+    8i + 2(t%4) + {0,1} (loads) and columns 4i + t%4 (stores)."""
+    import numpy as np
+    g = torch.Generator(device="cuda").manual_seed(11)
+    a = torch.randn(64, 192, device="cuda", generator=g).to(torch.bfloat16)
+    b = torch.randn(64, 192, device="cuda", generator=g).to(torch.bfloat16)
+    from asymmetric_kv_paged_gb300 import binding as B
+    d = torch.zeros(6144, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.attn_debug_tc_gemm(5, 0, 1, 64, a, b, d, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = (a.float() @ b.float().T).cpu().numpy()
+    got = d.cpu().numpy()
+    ld = got[:4096].reshape(4, 32, 32)
+    tol = 1e-3 * np.abs(ref).max()
+    for w in range(4):
+        for t in range(32):
+            for i in range(8):
+                for h in range(2):
+                    row = 16 * w + t // 4 + 8 * h
+                    for e in range(2):
+                        col = 8 * i + 2 * (t % 4) + e
+                        assert abs(ld[w, t, 4 * i + 2 * h + e] - ref[row, col]) < tol, (w, t, i, h, e)
+    stv = got[4096:].reshape(4, 32, 16)
+    for w in range(4):
+        for lane in range(16):
+            for col in range(16):
+                i, tq = divmod(col, 4)
+                h, tr = divmod(lane, 8)
+                t = 4 * tr + tq
+                assert stv[w, lane, col] == float(w * 100000 + t * 100 + 2 * i + h), (w, lane, col)
