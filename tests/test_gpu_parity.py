@@ -85,6 +85,9 @@ SMALL = [
     ("fp8_verify_sinks", [1500, 700], [8, 8], 16, 2, 16, 0, True, "fp8"),
     ("fp8_prefill", [900], [256], 64, 4, 128, 0, False, "fp8"),
     ("fp8_swa", [800, 300], [8, 1], 16, 2, 128, 128, True, "fp8"),
+    # gathered (page sizes TMA cannot tile) with blocks of more than 64 rows: M = 128
+    ("prefill_p1_gather", [600], [100], 8, 1, 1, 0, True, "bf16"),
+    ("fp8_prefill_p3_gather", [500, 90], [80, 3], 16, 2, 3, 0, False, "fp8"),
 ]
 
 
@@ -213,3 +216,15 @@ def test_parity_named_config(name):
     else:
         count = {"c5_chunked_prefill": 96}.get(name, 128)
         run_and_check(w, rows=sampled_rows(w, count, seed=zlib.crc32(name.encode()) % 1000))
+
+
+def test_batch_without_query_rows():
+    """Every request has zero new tokens: planning and running succeed and launch
+    nothing that touches the (empty) outputs."""
+    from asymmetric_kv_paged_gb300 import binding as B
+    w = W.make_workload(13, [40, 70], [0, 0], hq=8, hkv=2, page_size=16)
+    dw = _runner()(w)
+    assert dw.plan.workspace_bytes == 0
+    dw.run()
+    torch.cuda.synchronize()
+    assert B.attn_get_device_error(dw.plan) == 0
