@@ -22,7 +22,8 @@ ATTN_KV_FP8_E4M3 = 1
 
 EXPORTED = ("attn_plan", "attn_run_paged", "attn_run_phase", "attn_plan_destroy", "attn_get_device_error",
             "attn_status_string", "attn_plan_host", "attn_plan_info", "attn_plan_blocks",
-            "attn_plan_segments", "attn_debug_tc_gemm", "attn_run_paged_no_workspace")
+            "attn_plan_segments", "attn_debug_tc_gemm", "attn_run_paged_no_workspace",
+            "attn_append_kv")
 
 
 class attn_problem_t(ctypes.Structure):
@@ -65,6 +66,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                  ctypes.c_float, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp]
     L.attn_run_phase.argtypes = [vp, ctypes.c_int32] + L.attn_run_paged.argtypes[1:]
     L.attn_run_paged_no_workspace.argtypes = L.attn_run_paged.argtypes[:14] + [vp]
+    L.attn_append_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp]
     L.attn_plan_destroy.argtypes = [vp]
     L.attn_get_device_error.argtypes = [vp, vp, i32p]
     L.attn_status_string.argtypes = [ctypes.c_int]
@@ -195,6 +197,21 @@ def attn_run_paged_no_workspace(plan: Plan, q, k_cache, v_cache, page_table, seq
     args = args[:13] + args[15:]        # drop the workspace pointer and size
     _check(load().attn_run_paged_no_workspace(ctypes.c_void_p(plan.handle), *args),
            "attn_run_paged_no_workspace")
+
+
+def attn_append_kv(plan: Plan, k_new, v_new, k_cache, v_cache, page_table, seq_lens, qo_indptr,
+                   k_scale: float = 1.0, v_scale: float = 1.0, stream=None) -> None:
+    """Write the plan's new tokens' K/V rows into the paged caches (FP8 caches
+    get E4M3 codes of value / scale)."""
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    _check(load().attn_append_kv(ctypes.c_void_p(plan.handle), _ptr(k_new), _ptr(v_new),
+                                 _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seq_lens),
+                                 _ptr(qo_indptr), float(k_scale), float(v_scale),
+                                 ctypes.c_void_p(int(stream))), "attn_append_kv")
 
 
 def attn_get_device_error(plan: Plan) -> int:

@@ -162,6 +162,34 @@ attn_status_t attn_run_phase(attn_plan_t plan, int32_t phase, const void *q,
                              void *stream);
 
 /*
+ * Write the new tokens' K and V rows into the paged caches — the step that
+ * precedes attention on every mode.  For request b and its new token t
+ * (qo_indptr[b] <= tok = qo_indptr[b] + t < qo_indptr[b+1]) the position is
+ * i = seq_lens[b] - n_b + t (the new tokens are the last n_b keys, as for
+ * attn_run_paged), stored at page page_table[b][i / P], offset i % P, for
+ * every KV head g:
+ *   BF16 caches: k_cache[page][i % P][g][:] = k_new[tok][g][:] bit for bit;
+ *   FP8 caches:  k_cache[...] = E4M3(k_new[tok][g][:] / k_scale), the
+ *                division in fp32 (IEEE, round to nearest even) and the E4M3
+ *                rounding to nearest even with saturation to +-448, which is
+ *                how an FP8 E4M3 KV cache with a per-tensor scale stores its
+ *                entries (model card MiMo-V2.6-Flash-RL-FP8KV-W4A8-2x-RTX-PRO-
+ *                6000, "What the kernels do"); V likewise with v_scale.
+ *   k_new, v_new bf16 [total_q][Hkv][192] and [total_q][Hkv][128], contiguous.
+ *   k_cache, v_cache, page_table, seq_lens, qo_indptr: as for attn_run_paged
+ *                (device copies equal to the plan's host arrays).
+ *   k_scale, v_scale  finite and > 0 for FP8 caches; ignored for BF16.
+ * Only the written slots change.  A page id outside [0, num_pages) is not
+ * dereferenced: that token's rows are skipped and the plan's device error
+ * word records it.  Runs on `stream`; no allocation, no synchronisation.
+ * Errors: INVALID_ARG, CUDA.
+ */
+attn_status_t attn_append_kv(attn_plan_t plan, const void *k_new, const void *v_new,
+                             void *k_cache, void *v_cache, const int32_t *page_table,
+                             const int32_t *seq_lens, const int32_t *qo_indptr, float k_scale,
+                             float v_scale, void *stream);
+
+/*
  * Size of the library-owned scratch used by attn_run_paged_no_workspace.
  */
 #define ATTN_NO_WORKSPACE_MAX_BYTES (16u * 1024u * 1024u)
