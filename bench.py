@@ -323,6 +323,55 @@ def cpu_baseline(w, budget_s: float = 12.0):
                       f"{t_total:.1f} s FP64 on host cores"}
 
 
+def measure_append(name: str, pk: dict, steps: int, warmup: int):
+    """attn_append_kv on the new tokens of a named workload: their K/V rows read
+    (bf16) and written into the pages (bf16 or E4M3) once, plus the page-table
+    entries, lengths and offsets read; L2 flushed between steps."""
+    import torch
+    from asymmetric_kv_paged_gb300 import binding, workloads
+    from asymmetric_kv_paged_gb300.runner import DeviceWorkload
+    w = workloads.named(name)
+    dw = DeviceWorkload(w, device=torch.cuda.current_device(), with_lse=False)
+    rng = np.random.default_rng(99)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    kn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, DQK), dtype=np.float32)).to(
+        dev).to(torch.bfloat16)
+    vn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, DV), dtype=np.float32)).to(
+        dev).to(torch.bfloat16)
+    es = 2 if w.kv_dtype == "bf16" else 1
+    nbytes = (w.total_q * w.hkv * (DQK + DV) * (2 + es) + w.total_q * 4 * 3
+              + (w.batch + 1) * 4 + w.batch * 4)
+    ks, vs = (w.k_scale, w.v_scale) if w.kv_dtype == "fp8" else (1.0, 1.0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        binding.attn_append_kv(dw.plan, kn, vn, dw.k_cache, dw.v_cache, dw.page_table,
+                               dw.seq_lens, dw.qo_indptr, ks, vs, stream)
+
+    for _ in range(warmup):
+        step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for k in range(steps):
+        flush.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    assert binding.attn_get_device_error(dw.plan) == 0
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    out = {"workload": f"kv_append_{name}", "value": achieved, "unit": "GB/s", "ms_per_step": ms,
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                        "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None},
+           "algorithmic_bytes": nbytes, "tokens": w.total_q, "kv_dtype": w.kv_dtype,
+           "l2": "flushed between steps"}
+    del dw
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_extra(name: str, pk: dict, steps: int, warmup: int, world: int):
     import torch
     from asymmetric_kv_paged_gb300 import workloads
@@ -409,6 +458,10 @@ def run_ours(args):
             if name == args.workload:
                 continue
             extra.append(measure_extra(name, pk, max(20, args.steps // 4), args.warmup, 1))
+        # the KV-append step before attention: the headline decode's 32 tokens and
+        # the prefill chunk's 4096 (E4M3)
+        for name in ("c2_batched_decode", "c5_chunked_prefill"):
+            extra.append(measure_append(name, pk, max(20, args.steps // 4), args.warmup))
         line["extra"] = extra
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
