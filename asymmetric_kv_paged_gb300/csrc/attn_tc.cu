@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and fills the slot ring up to kSlotRing tiles ahead of the converters,
       // four tiles per round trip to memory: each lane looks up two keys of
       // each of the four tiles before storing any of them.
-      constexpr int R = Lay::kSlotRing;
+      constexpr int R = Lay::kSlotRing > 0 ? Lay::kSlotRing : 1;   // 0 in TMA kernels (unused)
       constexpr int kBatchTiles = 4;
       const int ln = tid & 31;
       int64_t *ring = reinterpret_cast<int64_t *>(smem + Lay::kOffSlots);
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       uint4 buf[kPer];
       {
-        constexpr int R = Lay::kSlotRing;
+        constexpr int R = Lay::kSlotRing > 0 ? Lay::kSlotRing : 1;   // 0 in TMA kernels (unused)
         const int r = k % R;
         if (!tc::mbar_wait_warp(&slot_bars->full[r], (k / R) & 1, &abort_flag)) break;
         const int64_t slot = reinterpret_cast<const int64_t *>(smem + Lay::kOffSlots)[r * kN + (ct >> 1)];
