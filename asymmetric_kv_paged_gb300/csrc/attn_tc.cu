@@ -6,12 +6,14 @@
 // row r <-> (token r / G, head g*G + r % G), so every draft token and every
 // head of the group shares one pass over the keys ("one program per whole
 // verify", and the 8-token x 16-head packing of the prefill kernel on the
-// MiMo-V2.6-Flash-RL model card, "What the kernels do").  Blocks with fewer
-// than 128 rows (decode: G rows) still issue M=128 MMAs: the tensor pipe has
-// time to spare while the tile streams in from HBM.
+// MiMo-V2.6-Flash-RL model card, "What the kernels do").  When no block has
+// more than 64 rows the kernel issues M=64 MMAs (smaller Q tile: a fourth K/V
+// stage and a second Q buffer fit); blocks smaller than the MMA are copied
+// across its rows, each copy taking a slice of every key tile.
 //
 // Warp roles (352 threads):
-//   warps 0-3  softmax + epilogue: thread r owns row r (= TMEM lane r);
+//   warps 0-3  softmax + epilogue: MMA row p lives in TMEM lane p (M=128) or
+//              in lane 32*(p/16) + p%16 (M=64), and that lane's thread owns it;
 //   warps 4-7  converters: stage Q per block; turn raw FP8 K/V tiles into
 //              exact fp16 operand tiles; zero V rows of keys outside the
 //              block's range on edge tiles (unused slots may hold NaN:
@@ -20,7 +22,8 @@
 //   warp  8    TMEM allocation; issues the S = Q.K^T MMAs (one thread);
 //   warp  9    TMA producer: page-table lookup, then 3D tensor-map loads of
 //              the K/V boxes (BF16: straight into the 128-byte swizzled
-//              operand layout; FP8: raw rows into a staging ring);
+//              operand layout; FP8: raw rows into a staging ring); for the
+//              gather path, the page lookups into a ring of resolved slots;
 //   warp 10    issues the O += P.V MMAs (one thread).
 // TMEM: S double buffer (2 x 64 columns), O (128 columns), P double buffer (2 x 32).
 // Every wait is bounded in time; a broken invariant ends the kernel with bit 1
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (k >= NT && !tc::mbar_wait(empty, ((k / NT) - 1) & 1, &abort_flag)) break;
         // BF16: a tile with keys outside the block's range lands on edge_full, which
         // only the converters wait on (they zero those V rows); every other tile
-        // lands on tma_full, which only the MMA warp waits on.
+        // lands on tma_full, which only the Q.K^T issuer waits on.
         const bool edge = !FP8 && (key0 < bd.klo || key0 + kN > bd.khi);
         uint64_t *full = edge ? &bars.edge_full[t] : &bars.tma_full[t];
         mbar_expect_tx(full, kTileBytes);
@@ -509,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t *op = smem + Lay::kOffOp + s * kOpBytes;
       if (TMA && !FP8) {
         // BF16 tile landed by TMA in operand layout.  Interior tiles go straight
-        // to the MMA warp; on edge tiles zero the V rows outside the range first.
+        // to the Q.K^T issuer; on edge tiles zero the V rows outside the range first.
         if (key0 >= bd.klo && key0 + kN <= bd.khi) continue;
         if (!tc::mbar_wait(&bars.edge_full[s], (edge_parity >> s) & 1, &abort_flag)) break;
         edge_parity ^= 1u << s;
@@ -704,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sync_phase ^= 1;
       return ok;
     };
-    // One key tile: S slice from TMEM -> mask -> P slice to smem.
+    // One key tile: S slice from TMEM -> mask -> P slice to TMEM.
     // A thread owns nc (16, 32 or 64) key columns of its row, read from TMEM in
     // 16-column chunks; the load of chunk c+1 is in flight while chunk c is
     // processed.  The loops are not unrolled beyond that pair, so this hot code
