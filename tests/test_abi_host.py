@@ -162,3 +162,22 @@ def test_small_blocks_are_not_split_when_ctas_suffice():
     plan = B.attn_plan_host(prob, 100, keep)
     info = B.attn_plan_info(plan)
     assert info["ctas"] <= 100 and info["segments"] >= info["blocks"]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_schedule_invariants_on_random_problems(seed):
+    # seeded random shapes: ragged lengths, empty requests, every page size
+    # class (gather, divisor, multiple), windows, GQA ratios and SM counts
+    rng = np.random.default_rng(1000 + seed)
+    batch = int(rng.integers(1, 24))
+    hkv = int(rng.choice([1, 2, 4]))
+    hq = hkv * int(rng.choice([1, 2, 8, 16]))
+    P = int(rng.choice([1, 3, 16, 64, 128]))
+    n = rng.integers(0, 40, batch)
+    n[rng.random(batch) < 0.5] = 1
+    seq = n + rng.integers(0, 3000, batch)
+    seq = np.maximum(seq, 1)
+    win = int(rng.choice([0, 0, 1, 17, 128]))
+    num_sms = int(rng.choice([1, 7, 64, 152]))
+    w = W.make_workload(seed, seq.tolist(), n.tolist(), hq=hq, hkv=hkv, page_size=P, window=win)
+    _coverage_check(w, num_sms)
