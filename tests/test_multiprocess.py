@@ -41,7 +41,7 @@ def _rank_main(rank: int, world: int, port: int, results):
 
 def test_two_gloo_ranks_agree_on_the_slowest_step():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), results), nprocs=world, join=True)
         got = dict(results)
