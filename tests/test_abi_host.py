@@ -181,3 +181,19 @@ def test_schedule_invariants_on_random_problems(seed):
     num_sms = int(rng.choice([1, 7, 64, 152]))
     w = W.make_workload(seed, seq.tolist(), n.tolist(), hq=hq, hkv=hkv, page_size=P, window=win)
     _coverage_check(w, num_sms)
+
+
+def test_headers_compile_as_plain_c(tmp_path):
+    # the boundary is a C ABI: both headers must stand alone in C99, with no
+    # CUDA or C++ header behind them
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "abi.c"
+    src.write_text('#include "attn_paged.h"\n#include "attn_paged_debug.h"\n'
+                   "int main(void) { attn_plan_t p = 0; attn_problem_t q; (void)p; (void)q;\n"
+                   "  return ATTN_OK; }\n")
+    inc = os.path.join(ROOT, "include")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{inc}",
+                    "-fsyntax-only", str(src)], check=True)
