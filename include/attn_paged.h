@@ -114,10 +114,15 @@ attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *
  *   k_cache      [num_pages, P, Hkv, 192] of bf16 or E4M3 bytes.
  *   v_cache      [num_pages, P, Hkv, 128] of the same type.
  *   page_table   int32 [B, page_table_stride]; entries at or beyond
- *                ceil(seq_lens[b] / P) are never read.  Page ids outside
- *                [0, num_pages) are not dereferenced: the rows they would
- *                supply are read as zero and the plan's device error word
- *                records the fault (attn_get_device_error).
+ *                ceil(seq_lens[b] / P) are never read, and with a window
+ *                neither are the entries below floor(lo_b / P), where
+ *                lo_b = max(0, seq_lens[b] - n_b - window + 1) is the first key
+ *                request b's first query sees: a cache that evicts pages
+ *                behind the window may leave anything there (-1 included).
+ *                Page ids outside [0, num_pages) that are read are not
+ *                dereferenced: the rows they would supply are read as zero
+ *                and the plan's device error word records the fault
+ *                (attn_get_device_error).
  *   seq_lens     int32 [B] device copy; qo_indptr int32 [B+1] device copy.
  *                Both must equal the host arrays the plan was built from: the
  *                kernels take lengths from the plan's own device copy.

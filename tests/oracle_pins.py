@@ -251,6 +251,37 @@ def pin_nan_independence(o):
         assert np.array_equal(out0, out1) and np.array_equal(lse0, lse1)
 
 
+def drop_unseen_pages(w):
+    """The table with every page that holds no key the request's queries can see
+    (wholly below the window, or past the last key) replaced by -1, as a cache
+    that evicts such pages would leave it; also the number of pages dropped below
+    the window."""
+    pt = w.page_table.copy()
+    P = w.page_size
+    below = 0
+    for b in range(w.batch):
+        lo, L = w.visible_range(b)
+        pt[b, :lo // P] = -1
+        pt[b, -(-L // P):] = -1
+        below += lo // P
+    return pt, below
+
+
+def pin_evicted_pages_unread(o):
+    """Pages that no query of a request can see are never looked up: dropping them
+    from the table (-1, outside the pool) changes nothing.  With page size 1 the
+    page just below the window is dropped too, so one key too many is caught."""
+    for seed, P, win, kv in ((95, 4, 5, "bf16"), (96, 1, 3, "fp8"), (97, 8, 16, "bf16")):
+        w = make_workload(seed, [60, 33, 17], [1, 8, 3], hq=4, hkv=2, page_size=P,
+                          window=win, sinks=True, kv_dtype=kv)
+        pb = w.host_arrays()
+        out0, lse0 = o.attn_paged(pb)
+        pt, below = drop_unseen_pages(w)
+        assert below > 0
+        out1, lse1 = o.attn_paged(dict(pb, page_table=pt))
+        assert np.array_equal(out0, out1) and np.array_equal(lse0, lse1)
+
+
 def pin_hand_golden(o):
     """The hand-derived two-key case in tests/golden/hand_two_keys.json."""
     with open(os.path.join(GOLDEN, "hand_two_keys.json")) as f:
@@ -284,4 +315,5 @@ def pin_hand_golden(o):
 ALL_PINS = [pin_e4m3_table, pin_bf16_widening, pin_brute_force, pin_uniform_logits,
             pin_single_key, pin_sink_minus_inf, pin_window_ge_len, pin_split_merge,
             pin_page_permutation, pin_head_duplication, pin_mode_consistency,
-            pin_scale_invariance, pin_kv_scales, pin_nan_independence, pin_hand_golden]
+            pin_scale_invariance, pin_kv_scales, pin_nan_independence, pin_evicted_pages_unread,
+            pin_hand_golden]

@@ -197,6 +197,49 @@ def test_bad_page_id_sets_error_word():
     assert torch.isfinite(dw.out.float()).all()
 
 
+# Per-rank shapes under 8-way tensor parallelism.  The pages test "TP8 per-rank
+# shapes for hidden sizes 4096 and 6144" (sglang PR #41886, "Accuracy Tests")
+# without giving head counts; 64 to 128 q heads over 8 ranks, with the KV heads
+# split or replicated, gives 8 to 16 q heads and 1 or 2 KV heads per rank.
+TP8_SHAPES = [(8, 1), (12, 1), (16, 1), (16, 2)]
+TP8_MODES = [
+    # name, seq_lens, n, P, window, sinks
+    ("decode", [1000, 129, 2900, 64, 700], [1] * 5, 128, 0, False),
+    ("verify", [1500, 300, 77], [8, 8, 8], 16, 0, False),
+    ("swa_sinks", [700, 700, 260, 900], [1, 8, 8, 1], 128, 128, True),
+]
+
+
+@pytest.mark.parametrize("mode", TP8_MODES, ids=[m[0] for m in TP8_MODES])
+@pytest.mark.parametrize("shape", TP8_SHAPES, ids=lambda s: f"hq{s[0]}_hkv{s[1]}")
+def test_parity_tp8_rank_shapes(shape, mode):
+    hq, hkv = shape
+    name, seq, n, P, win, sinks = mode
+    w = W.make_workload(zlib.crc32(f"tp8_{hq}_{hkv}_{name}".encode()) % 1000, seq, n, hq=hq,
+                        hkv=hkv, page_size=P, window=win, sinks=sinks,
+                        name=f"tp8_{name}_hq{hq}_hkv{hkv}")
+    run_and_check(w)
+
+
+@pytest.mark.parametrize("P,kv", [(1, "bf16"), (3, "fp8"), (16, "bf16"), (16, "fp8"),
+                                  (128, "bf16"), (128, "fp8")])
+def test_evicted_pages_are_never_read(P, kv):
+    """A sliding-window cache may drop the pages that no query of a request can
+    see: entries of -1 there are never looked up, so the output keeps its bits
+    and the device error word stays clear."""
+    from oracle_pins import drop_unseen_pages
+    w = W.make_workload(14 + P, [1500, 700, 3000, 129], [1, 8, 3, 8], hq=16, hkv=2,
+                        page_size=P, window=200, sinks=True, kv_dtype=kv)
+    full = run_and_check(w)
+    w.page_table, below = drop_unseen_pages(w)
+    assert below > 0
+    dw = _runner()(w)
+    dw.run()
+    torch.cuda.synchronize()
+    assert torch.equal(full.out, dw.out) and torch.equal(full.lse, dw.lse)
+    assert B_err(dw) == 0
+
+
 # ---- full-size workloads, in the benchmark's launch configuration ----
 
 def sampled_rows(w, count, seed):
