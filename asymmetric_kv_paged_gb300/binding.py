@@ -23,7 +23,8 @@ ATTN_KV_FP8_E4M3 = 1
 EXPORTED = ("attn_plan", "attn_run_paged", "attn_run_phase", "attn_plan_destroy", "attn_get_device_error",
             "attn_status_string", "attn_plan_host", "attn_plan_info", "attn_plan_blocks",
             "attn_plan_segments", "attn_debug_tc_gemm", "attn_run_paged_no_workspace",
-            "attn_append_kv")
+            "attn_append_kv", "attn_plan_replayable", "attn_plan_replayable_host",
+            "attn_plan_replan_host", "attn_plan_fetch_device")
 
 
 class attn_problem_t(ctypes.Structure):
@@ -75,6 +76,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_plan_info.argtypes = [vp, i32p]
     L.attn_plan_blocks.argtypes = [vp, i32p]
     L.attn_plan_segments.argtypes = [vp, i32p]
+    L.attn_plan_replayable.argtypes = L.attn_plan.argtypes
+    L.attn_plan_replayable_host.argtypes = L.attn_plan_host.argtypes
+    L.attn_plan_replan_host.argtypes = [vp, i32p, i32p]
+    L.attn_plan_fetch_device.argtypes = [vp]
     L.attn_debug_tc_gemm.argtypes = [ctypes.c_int32] * 4 + [vp, vp, vp, vp, vp]
     for name in EXPORTED:
         if name != "attn_status_string":
@@ -144,6 +149,40 @@ def attn_plan_host(problem: attn_problem_t, num_sms: int, keep=None) -> Plan:
     _check(load().attn_plan_host(ctypes.byref(problem), int(num_sms), ctypes.byref(h)),
            "attn_plan_host")
     return Plan(h.value, 0, -1, keep)
+
+
+def attn_plan_replayable(bounds: attn_problem_t, device: int, keep=None) -> Plan:
+    """A plan whose lengths are read on the device at every run (seq_lens in
+    `bounds` are upper bounds; the query layout is fixed)."""
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(load().attn_plan_replayable(ctypes.byref(bounds), int(device), ctypes.byref(h),
+                                       ctypes.byref(ws)), "attn_plan_replayable")
+    return Plan(h.value, ws.value, device, keep)
+
+
+def attn_plan_replayable_host(bounds: attn_problem_t, num_sms: int, keep=None) -> Plan:
+    h = ctypes.c_void_p()
+    _check(load().attn_plan_replayable_host(ctypes.byref(bounds), int(num_sms), ctypes.byref(h)),
+           "attn_plan_replayable_host")
+    return Plan(h.value, 0, -1, keep)
+
+
+def attn_plan_replan_host(plan: Plan, seq_lens) -> int:
+    """Rebuild a replayable plan's host work list for `seq_lens`; returns the
+    device error bits the lengths would raise."""
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    err = ctypes.c_int32()
+    _check(load().attn_plan_replan_host(ctypes.c_void_p(plan.handle),
+                                        sl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                        ctypes.byref(err)), "attn_plan_replan_host")
+    return err.value
+
+
+def attn_plan_fetch_device(plan: Plan) -> None:
+    """Copy the work list the device planner last wrote into the host copy."""
+    _check(load().attn_plan_fetch_device(ctypes.c_void_p(plan.handle)), "attn_plan_fetch_device")
 
 
 def attn_plan_destroy(plan: Plan) -> None:

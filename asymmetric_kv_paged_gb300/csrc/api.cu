@@ -5,11 +5,14 @@
 
 #include <cmath>
 #include <cstring>
+#include <algorithm>
 #include <new>
+#include <vector>
 
 #include "attn_paged.h"
 #include "kernels.hpp"
 #include "plan.hpp"
+#include "replan.hpp"
 
 namespace {
 
@@ -69,12 +72,17 @@ void free_device(attn_plan_s *p) {
 
 attn_status_t upload(attn_plan_s *p) {
   const akp::HostPlan &hp = p->host;
+  const size_t nsegs = std::max<size_t>(hp.segs.size(), (size_t)hp.seg_capacity);
   const size_t b_bytes = align256(hp.blocks.size() * sizeof(akp::BlockDesc));
-  const size_t s_bytes = align256(hp.segs.size() * sizeof(akp::SegDesc));
+  const size_t s_bytes = align256(nsegs * sizeof(akp::SegDesc));
   const size_t c_bytes = align256(hp.cta_seg_begin.size() * sizeof(int32_t));
   const size_t m_bytes = align256(hp.merge_items.size() * sizeof(akp::MergeItem));
   const size_t e_bytes = 256;
-  const size_t total = b_bytes + s_bytes + c_bytes + m_bytes + e_bytes;
+  // replayable plans: the length bounds and two scratch arrays of the planner
+  const size_t r_bytes = hp.replayable ? align256(hp.seq_lens.size() * sizeof(int32_t)) +
+                                             2 * align256((hp.blocks.size() + 1) * sizeof(int32_t))
+                                       : 0;
+  const size_t total = b_bytes + s_bytes + c_bytes + m_bytes + e_bytes + r_bytes;
   uint8_t *base = nullptr;
   if (cudaMalloc(&base, total) != cudaSuccess) return ATTN_ERR_CUDA;
   p->dev.blocks = reinterpret_cast<akp::BlockDesc *>(base);
@@ -82,6 +90,14 @@ attn_status_t upload(attn_plan_s *p) {
   p->dev.cta_seg_begin = reinterpret_cast<int32_t *>(base + b_bytes + s_bytes);
   p->dev.merge_items = reinterpret_cast<akp::MergeItem *>(base + b_bytes + s_bytes + c_bytes);
   p->dev.err = reinterpret_cast<int32_t *>(base + b_bytes + s_bytes + c_bytes + m_bytes);
+  if (hp.replayable) {
+    uint8_t *r = base + b_bytes + s_bytes + c_bytes + m_bytes + e_bytes;
+    p->dev.seq_bounds = reinterpret_cast<int32_t *>(r);
+    r += align256(hp.seq_lens.size() * sizeof(int32_t));
+    p->dev.tile_start = reinterpret_cast<int32_t *>(r);
+    r += align256((hp.blocks.size() + 1) * sizeof(int32_t));
+    p->dev.part_start = reinterpret_cast<int32_t *>(r);
+  }
   cudaError_t e = cudaSuccess;
   if (!hp.blocks.empty())
     e = cudaMemcpy(p->dev.blocks, hp.blocks.data(), hp.blocks.size() * sizeof(akp::BlockDesc),
@@ -95,6 +111,9 @@ attn_status_t upload(attn_plan_s *p) {
   if (e == cudaSuccess && !hp.merge_items.empty())
     e = cudaMemcpy(p->dev.merge_items, hp.merge_items.data(),
                    hp.merge_items.size() * sizeof(akp::MergeItem), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && hp.replayable && !hp.seq_lens.empty())
+    e = cudaMemcpy(p->dev.seq_bounds, hp.seq_lens.data(), hp.seq_lens.size() * sizeof(int32_t),
+                   cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(p->dev.err, 0, e_bytes);
   if (e == cudaSuccess) e = akp::prepare_attn_tc(hp);
   if (e != cudaSuccess) {
@@ -108,13 +127,15 @@ attn_status_t upload(attn_plan_s *p) {
 
 extern "C" {
 
-attn_status_t attn_plan_host(const attn_problem_t *problem, int32_t num_sms, attn_plan_t *plan) {
+static attn_status_t plan_host(const attn_problem_t *problem, int32_t num_sms, bool replayable,
+                               attn_plan_t *plan) {
   if (!plan) return ATTN_ERR_INVALID_ARG;
   *plan = nullptr;
   if (!problem) return ATTN_ERR_INVALID_ARG;
   attn_plan_s *p = new (std::nothrow) attn_plan_s();
   if (!p) return ATTN_ERR_INVALID_ARG;
-  attn_status_t st = akp::build_host_plan(problem, num_sms, &p->host);
+  attn_status_t st = replayable ? akp::build_replayable_plan(problem, num_sms, &p->host)
+                                : akp::build_host_plan(problem, num_sms, &p->host);
   if (st != ATTN_OK) {
     delete p;
     return st;
@@ -124,8 +145,8 @@ attn_status_t attn_plan_host(const attn_problem_t *problem, int32_t num_sms, att
   return ATTN_OK;
 }
 
-attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *plan,
-                        size_t *workspace_bytes) {
+static attn_status_t plan_device(const attn_problem_t *problem, int device, bool replayable,
+                                 attn_plan_t *plan, size_t *workspace_bytes) {
   if (!plan) return ATTN_ERR_INVALID_ARG;
   *plan = nullptr;
   if (!problem || !workspace_bytes || device < 0) return ATTN_ERR_INVALID_ARG;
@@ -135,7 +156,7 @@ attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *
   if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return ATTN_ERR_CUDA;
   attn_plan_t p = nullptr;
-  attn_status_t st = attn_plan_host(problem, num_sms, &p);
+  attn_status_t st = plan_host(problem, num_sms, replayable, &p);
   if (st != ATTN_OK) return st;
   p->device = device;
   st = upload(p);
@@ -146,6 +167,25 @@ attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *
   *workspace_bytes = p->host.workspace_bytes;
   *plan = p;
   return ATTN_OK;
+}
+
+attn_status_t attn_plan_host(const attn_problem_t *problem, int32_t num_sms, attn_plan_t *plan) {
+  return plan_host(problem, num_sms, false, plan);
+}
+
+attn_status_t attn_plan_replayable_host(const attn_problem_t *bounds, int32_t num_sms,
+                                        attn_plan_t *plan) {
+  return plan_host(bounds, num_sms, true, plan);
+}
+
+attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *plan,
+                        size_t *workspace_bytes) {
+  return plan_device(problem, device, false, plan, workspace_bytes);
+}
+
+attn_status_t attn_plan_replayable(const attn_problem_t *bounds, int device, attn_plan_t *plan,
+                                   size_t *workspace_bytes) {
+  return plan_device(bounds, device, true, plan, workspace_bytes);
 }
 
 attn_status_t attn_plan_destroy(attn_plan_t plan) {
@@ -225,6 +265,22 @@ static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const
   DeviceGuard guard(cur == plan->device ? cur : plan->device);
   if (!guard.ok) return ATTN_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((phases & 1) && hp.replayable) {
+    akp::ReplanArgs r{};
+    r.blocks = plan->dev.blocks;
+    r.segs = plan->dev.segs;
+    r.cta_seg_begin = plan->dev.cta_seg_begin;
+    r.tile_start = plan->dev.tile_start;
+    r.part_start = plan->dev.part_start;
+    r.seq_lens = seq_lens;
+    r.seq_bounds = plan->dev.seq_bounds;
+    r.err = plan->dev.err;
+    r.nb = (int32_t)hp.blocks.size();
+    r.num_ctas = hp.num_ctas;
+    r.group = hp.group;
+    r.window = pr.window;
+    if (akp::launch_replan(r, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
   if ((phases & 1) && akp::launch_attn_tc(hp, a, maps, st) != cudaSuccess) return ATTN_ERR_CUDA;
   if ((phases & 2) && akp::launch_merge(hp, a, st) != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
@@ -300,6 +356,47 @@ attn_status_t attn_plan_blocks(attn_plan_t plan, int32_t *blocks_host) {
     std::memcpy(d, v, sizeof v);
     d += 8;
   }
+  return ATTN_OK;
+}
+
+attn_status_t attn_plan_replan_host(attn_plan_t plan, const int32_t *seq_lens_host,
+                                   int32_t *err) {
+  if (!plan || !plan->host.replayable || !err) return ATTN_ERR_INVALID_ARG;
+  if (!seq_lens_host && !plan->host.seq_lens.empty()) return ATTN_ERR_INVALID_ARG;
+  *err = akp::replan_host(&plan->host, seq_lens_host);
+  return ATTN_OK;
+}
+
+attn_status_t attn_plan_fetch_device(attn_plan_t plan) {
+  if (!plan || !plan->host.replayable || plan->device < 0) return ATTN_ERR_INVALID_ARG;
+  akp::HostPlan &hp = plan->host;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return ATTN_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  std::vector<akp::BlockDesc> blocks(hp.blocks.size());
+  std::vector<int32_t> begin(hp.cta_seg_begin.size());
+  if (!blocks.empty() &&
+      cudaMemcpy(blocks.data(), plan->dev.blocks, blocks.size() * sizeof(akp::BlockDesc),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (cudaMemcpy(begin.data(), plan->dev.cta_seg_begin, begin.size() * sizeof(int32_t),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const int32_t nsegs = begin.back();
+  if (nsegs < 0 || nsegs > hp.seg_capacity) return ATTN_ERR_CUDA;
+  std::vector<akp::SegDesc> segs(nsegs);
+  if (nsegs > 0 && cudaMemcpy(segs.data(), plan->dev.segs, segs.size() * sizeof(akp::SegDesc),
+                              cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  std::vector<int32_t> seg_cta(nsegs);
+  for (int32_t c = 0; c + 1 < (int32_t)begin.size(); ++c)
+    for (int32_t s = begin[c]; s < begin[c + 1] && s < nsegs; ++s) seg_cta[s] = c;
+  hp.multi_split_blocks = 0;
+  for (const akp::BlockDesc &b : blocks) hp.multi_split_blocks += b.num_splits > 1;
+  hp.blocks = std::move(blocks);
+  hp.cta_seg_begin = std::move(begin);
+  hp.segs = std::move(segs);
+  hp.seg_cta = std::move(seg_cta);
   return ATTN_OK;
 }
 

@@ -40,6 +40,10 @@ cudaError_t launch_attn_tc(const HostPlan &hp, const RunArgs &a, const TmaMaps &
 cudaError_t prepare_attn_tc(const HostPlan &hp);
 // Whether K/V tiles of this page size can be loaded as TMA boxes.
 bool tc_tma_page_size(int32_t page_size, int32_t num_pages);
+// Device planner of replayable plans (replan.cu): rewrites the work list
+// from the run's lengths; launched before the attention kernel.
+struct ReplanArgs;
+cudaError_t launch_replan(const ReplanArgs &r, cudaStream_t stream);
 // Log-sum-exp merge of multi-split blocks.
 cudaError_t launch_merge(const HostPlan &hp, const RunArgs &a, cudaStream_t stream);
 

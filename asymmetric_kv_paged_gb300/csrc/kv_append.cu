@@ -63,6 +63,10 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     const int b = lo;
     const int q0 = __ldg(a.qo_indptr + b), n = __ldg(a.qo_indptr + b + 1) - q0;
     const int64_t i = (int64_t)__ldg(a.seq_lens + b) - n + (tok - q0);
+    if (i < 0 || i / a.page_size >= a.pt_stride) {   // a length outside the table row
+      atomicOr(a.err, 4);
+      continue;
+    }
     const int32_t page = __ldg(a.page_table + (int64_t)b * a.pt_stride + i / a.page_size);
     if (page < 0 || page >= a.num_pages) {
       atomicOr(a.err, 1);

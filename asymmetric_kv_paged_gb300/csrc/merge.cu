@@ -29,6 +29,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 __global__ void __launch_bounds__(32 * kMergeRowsPerCta) merge_kernel(const RunArgs a) {
   const MergeItem it = a.merge_items[blockIdx.x];
   const BlockDesc bd = a.blocks[it.block];
+  if (bd.num_splits <= 1) return;   // a replayable plan's run left the block whole
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int r = it.row_begin + warp;

@@ -54,6 +54,11 @@ struct HostPlan {
   size_t workspace_bytes = 0;
   int32_t multi_split_blocks = 0;
   bool use_tma = false;          // K/V tiles as TMA boxes (else gathered by threads)
+  // Replayable plans: seq_lens holds the per-request upper bounds, the work
+  // list is rebuilt from each run's lengths (replan.hpp); segs, part_rows and
+  // merge_items are sized for any lengths within the bounds.
+  bool replayable = false;
+  int64_t seg_capacity = 0;
 };
 
 // Device-side copy of a plan (owned by attn_plan_s).
@@ -63,10 +68,25 @@ struct DevicePlan {
   int32_t *cta_seg_begin = nullptr;
   MergeItem *merge_items = nullptr;
   int32_t *err = nullptr;  // device error word
+  // replayable plans only
+  int32_t *seq_bounds = nullptr;   // [B]
+  int32_t *tile_start = nullptr;   // scratch [blocks + 1]
+  int32_t *part_start = nullptr;   // scratch [blocks + 1]
 };
 
 // Validate `p` and build the schedule for a device with num_sms SMs.
 attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan *out);
+
+// A replayable plan for the query layout of `p`, whose seq_lens are upper
+// bounds: the blocks of build_host_plan, one CTA per SM (at most one per key
+// tile), capacities for any lengths within the bounds, and the work list of
+// the bounds themselves.
+attn_status_t build_replayable_plan(const attn_problem_t *p, int32_t num_sms, HostPlan *out);
+
+// Host mirror of the device planner: rebuild a replayable plan's work list for
+// the lengths seq_lens[B], clamped into [n_b, bound_b] as on the device.
+// Returns the error bits the device planner would set (4: a length clamped).
+int32_t replan_host(HostPlan *hp, const int32_t *seq_lens);
 
 // Workspace carve-up: partial outputs then partial lse, each 256-B aligned.
 inline size_t part_o_bytes(int64_t part_rows) {

@@ -14,6 +14,7 @@
 #include <cstring>
 
 #include "plan.hpp"
+#include "replan.hpp"
 
 namespace akp {
 
@@ -161,6 +162,90 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   hp.workspace_bytes = hp.part_rows ? part_o_bytes(hp.part_rows) + part_lse_bytes(hp.part_rows) : 0;
   *out = std::move(hp);
   return ATTN_OK;
+}
+
+// Replayable plans trade the static dealing above (whole small blocks, slack)
+// for one a single CTA can redo on the device in microseconds: equal shares of
+// the tiles in block order (replan.hpp).
+attn_status_t build_replayable_plan(const attn_problem_t *p, int32_t num_sms, HostPlan *out) {
+  HostPlan hp;
+  attn_status_t st = build_host_plan(p, num_sms, &hp);
+  if (st != ATTN_OK) return st;
+  const int64_t nb = (int64_t)hp.blocks.size();
+  // no run has more tiles than this: khi never exceeds its value at the bounds
+  int64_t max_tiles = 0;
+  int32_t max_rows = 0;
+  for (const BlockDesc &bd : hp.blocks) {
+    max_tiles += (bd.khi - 1) / kKeyTile + 1;
+    max_rows = std::max(max_rows, bd.nrows);
+  }
+  if (max_tiles >= INT32_MAX / 2) return ATTN_ERR_UNSUPPORTED;
+  hp.replayable = true;
+  hp.num_ctas = (int32_t)std::min<int64_t>(num_sms, max_tiles);
+  hp.seg_capacity = nb + hp.num_ctas;
+  // a multi-split block keeps nrows partial rows per split, and there are at
+  // most nb + num_ctas - 1 segments in all
+  hp.part_rows = (int64_t)max_rows * hp.seg_capacity;
+  if (hp.part_rows > INT32_MAX / kDv) return ATTN_ERR_UNSUPPORTED;
+  hp.workspace_bytes = hp.part_rows ? part_o_bytes(hp.part_rows) + part_lse_bytes(hp.part_rows) : 0;
+  // merge items for every block: the merge skips blocks a run leaves whole
+  hp.merge_items.clear();
+  for (int64_t bi = 0; bi < nb; ++bi)
+    for (int32_t r = 0; r < hp.blocks[bi].nrows; r += kMergeRowsPerCta)
+      hp.merge_items.push_back(MergeItem{(int32_t)bi, r});
+  replan_host(&hp, hp.seq_lens.data());
+  *out = std::move(hp);
+  return ATTN_OK;
+}
+
+int32_t replan_host(HostPlan *hp, const int32_t *seq_lens) {
+  int32_t err = 0;
+  const int32_t nb = (int32_t)hp->blocks.size();
+  std::vector<int32_t> start(nb + 1, 0);
+  for (int32_t bi = 0; bi < nb; ++bi) {
+    BlockDesc &bd = hp->blocks[bi];
+    const int32_t bound = hp->seq_lens[bd.b];
+    int32_t L = seq_lens[bd.b];
+    if (L < bd.n || L > bound) {
+      err |= 4;
+      L = L < bd.n ? bd.n : bound;
+    }
+    int32_t klo, khi;
+    block_keys(bd, L, hp->group, hp->prob.window, &klo, &khi);
+    bd.L = L;
+    bd.klo = klo;
+    bd.khi = khi;
+    start[bi + 1] = start[bi] + block_tile_count(klo, khi);
+  }
+  const int64_t T = start[nb];
+  const int64_t ctas = std::min<int64_t>(T, hp->num_ctas);
+  hp->segs.clear();
+  hp->seg_cta.clear();
+  hp->cta_seg_begin.assign(hp->num_ctas + 1, 0);
+  for (int32_t c = 0; c < hp->num_ctas; ++c) {
+    if (c < ctas) {
+      const int64_t a = share_begin(c, T, ctas), e = share_begin(c + 1, T, ctas);
+      for (int32_t bi = block_at(start.data(), nb, a); bi < nb && start[bi] < e; ++bi) {
+        hp->segs.push_back(
+            share_segment(bi, hp->blocks[bi], start[bi], start[bi + 1], a, e, c, T, ctas));
+        hp->seg_cta.push_back(c);
+      }
+    }
+    hp->cta_seg_begin[c + 1] = (int32_t)hp->segs.size();
+  }
+  int64_t part = 0;
+  hp->multi_split_blocks = 0;
+  for (int32_t bi = 0; bi < nb; ++bi) {
+    BlockDesc &bd = hp->blocks[bi];
+    bd.num_splits = share_splits(start[bi], start[bi + 1], T, ctas);
+    bd.part_row_base = -1;
+    if (bd.num_splits > 1) {
+      bd.part_row_base = (int32_t)part;
+      part += (int64_t)bd.num_splits * bd.nrows;
+      hp->multi_split_blocks++;
+    }
+  }
+  return err;
 }
 
 }  // namespace akp

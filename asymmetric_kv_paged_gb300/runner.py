@@ -21,9 +21,10 @@ def _dev(a: np.ndarray, device, dtype=None) -> torch.Tensor:
 class DeviceWorkload:
     """A workload resident in device memory with its plan, output and workspace."""
 
-    def __init__(self, w, device: int = 0, with_lse: bool = True):
+    def __init__(self, w, device: int = 0, with_lse: bool = True, replayable: bool = False):
         self.w = w
         self.device = device
+        self.replayable = replayable    # w.seq_lens are then upper bounds
         dev = torch.device("cuda", device)
         self.q = _dev(w.q, dev, torch.bfloat16)
         kv_t = torch.bfloat16 if w.kv_dtype == "bf16" else torch.uint8
@@ -50,6 +51,8 @@ class DeviceWorkload:
 
     def make_plan(self):
         prob, keep = self.problem()
+        if self.replayable:
+            return B.attn_plan_replayable(prob, self.device, keep)
         return B.attn_plan(prob, self.device, keep)
 
     def run_phase(self, phase: int, stream=None) -> None:

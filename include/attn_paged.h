@@ -109,6 +109,27 @@ attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *
                         size_t *workspace_bytes);
 
 /*
+ * Build a replayable plan: one whose request lengths are read on the device
+ * at every run, so that a CUDA graph captured once keeps serving a batch while
+ * its requests grow (the decode and verify paths run under CUDA graph replay
+ * in sglang PR #41886, "Accuracy Tests").
+ *   bounds->qo_indptr_host   the batch's query layout, fixed for the plan's
+ *                            lifetime (the device qo_indptr must equal it).
+ *   bounds->seq_lens_host    per-request upper bounds of the lengths;
+ *                            page_table_stride must cover them.
+ * Other fields as for attn_plan.  Each run first launches a one-CTA planner
+ * kernel that reads the caller's device seq_lens and rewrites the plan's work
+ * list in device memory (key ranges, equal shares of the key tiles for one CTA
+ * per SM, splits, partial offsets); the attention kernel and the merge follow
+ * on the same stream.  The workspace reported covers every length vector
+ * within the bounds.  Results equal those of a plan built for the run's
+ * lengths, up to the floating-point order of the split merge.
+ * Synchronous; allocates device memory.  Errors as for attn_plan.
+ */
+attn_status_t attn_plan_replayable(const attn_problem_t *bounds, int device, attn_plan_t *plan,
+                                   size_t *workspace_bytes);
+
+/*
  * Run the planned attention on `stream`.
  *   q            bf16 [total_q, Hq, 192], row-major, contiguous.
  *   k_cache      [num_pages, P, Hkv, 192] of bf16 or E4M3 bytes.
@@ -125,7 +146,11 @@ attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *
  *                (attn_get_device_error).
  *   seq_lens     int32 [B] device copy; qo_indptr int32 [B+1] device copy.
  *                Both must equal the host arrays the plan was built from: the
- *                kernels take lengths from the plan's own device copy.
+ *                kernels take lengths from the plan's own device copy.  For a
+ *                replayable plan seq_lens is read at every run instead, and
+ *                may hold any n_b <= seq_lens[b] <= bound_b; a length outside
+ *                that range is clamped into it and sets bit 2 of the device
+ *                error word.
  *   sinks        fp32 [Hq] sink logits in the units of the scaled scores, or
  *                NULL; must be non-NULL exactly when the plan has_sinks.
  *   window       must equal the plan's window.
@@ -186,7 +211,9 @@ attn_status_t attn_run_phase(attn_plan_t plan, int32_t phase, const void *q,
  *   k_scale, v_scale  finite and > 0 for FP8 caches; ignored for BF16.
  * Only the written slots change.  A page id outside [0, num_pages) is not
  * dereferenced: that token's rows are skipped and the plan's device error
- * word records it.  Runs on `stream`; no allocation, no synchronisation.
+ * word records it (bit 0).  With a replayable plan seq_lens may change between
+ * runs; a position outside the request's page-table row is skipped and sets
+ * bit 2.  Runs on `stream`; no allocation, no synchronisation.
  * Errors: INVALID_ARG, CUDA.
  */
 attn_status_t attn_append_kv(attn_plan_t plan, const void *k_new, const void *v_new,
@@ -237,8 +264,11 @@ attn_status_t attn_plan_destroy(attn_plan_t plan);
 
 /*
  * Read and clear the plan's device error word (synchronous).  Bit 0: a page
- * id outside [0, num_pages) was met.  The workspace argument is unused and
- * may be NULL.
+ * id outside [0, num_pages) was met.  Bit 1: a pipeline wait of the attention
+ * kernel gave up after its time limit (the affected rows are not valid).
+ * Bit 2: a run length outside a replayable plan's bounds (clamped), or an
+ * appended position outside its page-table row (skipped).  The workspace
+ * argument is unused and may be NULL.
  */
 attn_status_t attn_get_device_error(attn_plan_t plan, void *workspace, int32_t *err);
 
@@ -251,7 +281,7 @@ const char *attn_status_string(attn_status_t status);
  * attn_plan_host builds a plan on the host only, for a device with `num_sms`
  * SMs; it cannot be run.  attn_plan_info reports its shape:
  *   info[0] = number of row blocks, info[1] = number of work segments,
- *   info[2] = number of CTAs, info[3] = rows per block (16, 64 or 128),
+ *   info[2] = number of CTAs, info[3] = rows per block (64 or 128),
  *   info[4] = key tile (keys per tile), info[5] = multi-split blocks,
  *   info[6] = workspace bytes (low 31 bits in info[6], high bits in info[7]).
  * attn_plan_blocks copies the blocks as 8 int32 each:
@@ -260,11 +290,26 @@ const char *attn_status_string(attn_status_t status);
  *   {cta, block, tile_begin, tile_end, split}
  * where tiles are absolute (tile T holds keys [T*tile, (T+1)*tile)).
  * The destination arrays must hold info[0]*8 (resp. info[1]*5) int32.
+ *
+ * attn_plan_replayable_host is attn_plan_replayable on the host only (the
+ * work list is that of the bounds).  attn_plan_replan_host rebuilds a
+ * replayable plan's host copy of the work list for the lengths
+ * seq_lens_host[B] with the device planner's arithmetic, and stores in *err
+ * the error bits the device would set (4: a length clamped into its bounds).
+ * attn_plan_fetch_device synchronises the plan's device and copies the work
+ * list the device planner last wrote into the host copy (replayable plans
+ * built by attn_plan_replayable).  All three: INVALID_ARG for other plans;
+ * attn_plan_fetch_device also CUDA.
  */
 attn_status_t attn_plan_host(const attn_problem_t *problem, int32_t num_sms, attn_plan_t *plan);
 attn_status_t attn_plan_info(attn_plan_t plan, int32_t info[8]);
 attn_status_t attn_plan_blocks(attn_plan_t plan, int32_t *blocks_host);
 attn_status_t attn_plan_segments(attn_plan_t plan, int32_t *segments_host);
+attn_status_t attn_plan_replayable_host(const attn_problem_t *bounds, int32_t num_sms,
+                                        attn_plan_t *plan);
+attn_status_t attn_plan_replan_host(attn_plan_t plan, const int32_t *seq_lens_host,
+                                    int32_t *err);
+attn_status_t attn_plan_fetch_device(attn_plan_t plan);
 
 #ifdef __cplusplus
 }

@@ -62,13 +62,23 @@ def test_plan_rejects_bad_problems(kw, status):
     assert e.value.status == status
 
 
-def _coverage_check(w, num_sms):
-    prob, keep = B.make_problem(
+def _problem_of(w, seq_lens=None):
+    return B.make_problem(
         batch=w.batch, num_q_heads=w.hq, num_kv_heads=w.hkv, page_size=w.page_size,
         num_pages=w.num_pages, page_table_stride=w.page_table.shape[1],
         kv_dtype=B.ATTN_KV_BF16, window=w.window, has_sinks=False, qo_indptr=w.qo_indptr,
-        seq_lens=w.seq_lens)
-    plan = B.attn_plan_host(prob, num_sms, keep)
+        seq_lens=w.seq_lens if seq_lens is None else seq_lens)
+
+
+def _coverage_check(w, num_sms):
+    prob, keep = _problem_of(w)
+    return _check_plan(B.attn_plan_host(prob, num_sms, keep), w, num_sms)
+
+
+def _check_plan(plan, w, num_sms):
+    """The plan's work list covers every (request, KV head, row) once, with the
+    key range its rows see, each block's tiles once in split order, and CTA
+    loads balanced; returns the plan's info."""
     info = B.attn_plan_info(plan)
     blocks = B.attn_plan_blocks(plan)
     segs = B.attn_plan_segments(plan)
@@ -197,3 +207,89 @@ def test_headers_compile_as_plain_c(tmp_path):
     inc = os.path.join(ROOT, "include")
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{inc}",
                     "-fsyntax-only", str(src)], check=True)
+
+
+# ---- replayable plans: the work list is rebuilt from each run's lengths ----
+
+def _random_bounds(seed):
+    rng = np.random.default_rng(2000 + seed)
+    batch = int(rng.integers(1, 20))
+    hkv = int(rng.choice([1, 2, 4]))
+    hq = hkv * int(rng.choice([1, 2, 8, 16]))
+    P = int(rng.choice([1, 3, 16, 64, 128]))
+    n = rng.integers(0, 40, batch)
+    n[rng.random(batch) < 0.5] = 1
+    bound = n + rng.integers(0, 3000, batch)
+    bound = np.maximum(bound, 1)
+    win = int(rng.choice([0, 0, 1, 17, 128]))
+    num_sms = int(rng.choice([1, 7, 64, 152]))
+    w = W.make_workload(seed, bound.tolist(), n.tolist(), hq=hq, hkv=hkv, page_size=P, window=win)
+    return w, n, bound, num_sms, rng
+
+
+def _with_lens(w, lens):
+    import copy
+    w2 = copy.copy(w)
+    w2.seq_lens = np.asarray(lens, np.int32)
+    return w2
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_replayable_replan_keeps_schedule_invariants(seed):
+    """For lengths anywhere within the bounds, the host mirror of the device
+    planner gives a valid work list: every row once, the key range of the run's
+    lengths, equal CTA shares, and the capacities the plan was sized for."""
+    w, n, bound, num_sms, rng = _random_bounds(seed)
+    prob, keep = _problem_of(w)
+    plan = B.attn_plan_replayable_host(prob, num_sms, keep)
+    info0 = B.attn_plan_info(plan)
+    assert info0["ctas"] <= num_sms
+    max_rows = max(int(nrows) for nrows in B.attn_plan_blocks(plan)[:, 3]) if info0["blocks"] else 0
+    cap_rows = max_rows * (info0["blocks"] + info0["ctas"])
+    for trial in range(6):
+        lens = n + (rng.random(w.batch) * (bound - n + 1)).astype(np.int64)
+        lens = np.minimum(lens, bound)
+        if trial == 0:
+            lens = bound.copy()
+        elif trial == 1:
+            lens = n.copy()                              # only the new tokens
+        assert B.attn_plan_replan_host(plan, lens) == 0
+        info = _check_plan(plan, _with_lens(w, lens), num_sms)
+        assert info["ctas"] == info0["ctas"] and info["blocks"] == info0["blocks"]
+        assert info["segments"] <= info["blocks"] + info["ctas"]
+        segs = B.attn_plan_segments(plan)
+        loads = np.bincount(segs[:, 0], weights=segs[:, 3] - segs[:, 2],
+                            minlength=info["ctas"]) if len(segs) else np.zeros(1)
+        busy = loads[loads > 0]
+        if len(busy):
+            assert busy.max() - busy.min() <= 1          # equal shares, rounded down
+            assert np.all(loads[:len(busy)] > 0)         # the working CTAs come first
+        blocks = B.attn_plan_blocks(plan)
+        multi = blocks[blocks[:, 6] > 1]
+        used = int((multi[:, 6] * multi[:, 3]).sum())
+        assert used <= cap_rows
+        if len(multi):
+            # partial rows packed in block order
+            ends = multi[:, 7] + multi[:, 6] * multi[:, 3]
+            assert multi[0, 7] == 0 and np.array_equal(multi[1:, 7], ends[:-1])
+
+
+def test_replayable_replan_clamps_lengths_and_matches_static_ranges():
+    w = W.make_workload(3, [500, 90, 1300], [8, 1, 3], hq=16, hkv=2, page_size=16, window=100)
+    prob, keep = _problem_of(w)
+    plan = B.attn_plan_replayable_host(prob, 152, keep)
+    first = B.attn_plan_blocks(plan).copy()
+    # lengths outside [n_b, bound_b] are clamped, and flagged like the device does
+    assert B.attn_plan_replan_host(plan, [4, 91, 2000]) == 4
+    clamped = B.attn_plan_blocks(plan).copy()
+    assert B.attn_plan_replan_host(plan, [8, 90, 1300]) == 0
+    assert np.array_equal(B.attn_plan_blocks(plan), clamped)
+    # the bounds themselves give back the plan as built
+    assert B.attn_plan_replan_host(plan, [500, 90, 1300]) == 0
+    assert np.array_equal(B.attn_plan_blocks(plan), first)
+    # key ranges are those of a static plan for the same lengths
+    for lens in ([200, 90, 1000], [8, 1, 3], [499, 77, 1299]):
+        assert B.attn_plan_replan_host(plan, lens) == 0
+        sprob, skeep = _problem_of(w, lens)
+        static = B.attn_plan_blocks(B.attn_plan_host(sprob, 152, skeep))
+        assert np.array_equal(B.attn_plan_blocks(plan)[:, :6], static[:, :6])
