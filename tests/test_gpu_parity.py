@@ -124,6 +124,44 @@ def test_v_path_bit_exact(P, kv):
         assert np.array_equal(got[:, h], expect[:, h // G]), f"head {h}"
 
 
+@pytest.mark.parametrize("P", [1, 16, 128])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_k_path_index_exact(P, kv):
+    """window 1 with n = L and one-hot queries: row t's only score is
+    scale * k_t[d], so lse / scale recovers column d of the K row the kernel
+    read.  Columns 0-2 of every key row hold base-16 digits of its position
+    (integers 1..16, exact in bf16 and E4M3) and column 3 its KV head, so
+    each (token, head) must name exactly its own key and head."""
+    L, hq, hkv = 300, 8, 2
+    G = hq // hkv
+    w = W.make_workload(21, [L], [L], hq=hq, hkv=hkv, page_size=P, window=1, kv_dtype=kv)
+    w.k_scale = 1.0
+    t = np.arange(L)
+    code = np.stack([t % 16 + 1, (t // 16) % 16 + 1, t // 256 + 1], axis=1)     # [L, 3]
+    slots = w.page_table[0, t // P].astype(np.int64) * P + t % P
+    kc = w.k_cache.reshape(-1, hkv, W.DQK).copy()
+    for g in range(hkv):
+        vals = np.concatenate([code, np.full((L, 1), g + 1)], axis=1).astype(np.float32)
+        if kv == "bf16":
+            kc[slots, g, :4] = W.bf16_bits(vals)
+        else:
+            kc[slots, g, :4] = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    w.k_cache = kc.reshape(w.k_cache.shape)
+    q = np.zeros((L, hq, W.DQK), np.float32)
+    for h in range(hq):
+        q[:, h, h % G] = 1.0
+    w.q = W.bf16_bits(q)
+    dw = _runner()(w)
+    dw.run()
+    torch.cuda.synchronize()
+    got = dw.lse.cpu().numpy().astype(np.float64) / w.softmax_scale          # [L, hq]
+    assert B_err(dw) == 0
+    for h in range(hq):
+        u, g = h % G, h // G
+        expect = code[:, u] if u < 3 else np.full(L, g + 1)
+        assert np.all(np.abs(got[:, h] - expect) < 1e-3), f"head {h}"
+
+
 def test_repeat_runs_bit_identical():
     w = W.make_workload(8, [3000, 1200], [8, 1], hq=16, hkv=2, page_size=128, sinks=True)
     dw = _runner()(w)
