@@ -25,6 +25,10 @@ CASES = [
     ("swa_sinks_p1", [1500, 800, 300], [1, 8, 1], 16, 2, 1, 128, True, "bf16"),
     ("prefill_gather_p3", [900], [200], 16, 2, 3, 0, False, "bf16"),
 ]
+# 8,400 blocks: the planner's scans run over several 1024-entry chunks, and its
+# 152 CTA shares each cover about 55 blocks
+_MANY = np.random.default_rng(77).integers(1, 41, 4200).tolist()
+CASES.append(("many_blocks", _MANY, [1] * len(_MANY), 4, 2, 16, 0, False, "bf16"))
 SHRINK = [777, 300, 65, 1, 0]     # replay at bound - d (at least n)
 
 
