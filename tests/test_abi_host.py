@@ -70,6 +70,64 @@ def _problem_of(w, seq_lens=None):
         seq_lens=w.seq_lens if seq_lens is None else seq_lens)
 
 
+def test_plan_rejects_bad_problems_beyond_shapes():
+    # element type outside the enum
+    prob, keep = _problem(kv_dtype=7)
+    with pytest.raises(B.AttnError) as e:
+        B.attn_plan_host(prob, 152, keep)
+    assert e.value.status == B.ATTN_ERR_UNSUPPORTED
+    # an empty pool, a negative batch, and host arrays missing for a batch
+    for kw in (dict(num_pages=0), dict(batch=-1)):
+        prob, keep = _problem(**kw)
+        with pytest.raises(B.AttnError) as e:
+            B.attn_plan_host(prob, 152, keep)
+        assert e.value.status == B.ATTN_ERR_INVALID_ARG
+    for field in ("qo_indptr_host", "seq_lens_host"):
+        prob, keep = _problem()
+        setattr(prob, field, None)
+        with pytest.raises(B.AttnError) as e:
+            B.attn_plan_host(prob, 152, keep)
+        assert e.value.status == B.ATTN_ERR_INVALID_ARG
+    # flat query rows x heads must stay within the kernels' int32 arithmetic
+    n = 2_000_000
+    prob, keep = _problem(batch=1, num_q_heads=64, num_kv_heads=4, page_table_stride=n // 16 + 1,
+                          num_pages=n // 16 + 2, qo_indptr=[0, n], seq_lens=[n])
+    with pytest.raises(B.AttnError) as e:
+        B.attn_plan_host(prob, 152, keep)
+    assert e.value.status == B.ATTN_ERR_UNSUPPORTED
+    # no SM count
+    prob, keep = _problem()
+    with pytest.raises(B.AttnError) as e:
+        B.attn_plan_host(prob, 0, keep)
+    assert e.value.status == B.ATTN_ERR_INVALID_ARG
+
+
+def test_replayable_plan_validates_and_sizes_for_the_bounds():
+    prob, keep = _problem(seq_lens=[100, 5])          # a bound below n
+    with pytest.raises(B.AttnError) as e:
+        B.attn_plan_replayable_host(prob, 152, keep)
+    assert e.value.status == B.ATTN_ERR_INVALID_ARG
+    # a batch with no query row plans to nothing and needs no workspace
+    prob, keep = _problem(qo_indptr=[0, 0, 0])
+    plan = B.attn_plan_replayable_host(prob, 152, keep)
+    info = B.attn_plan_info(plan)
+    assert info["blocks"] == info["segments"] == info["ctas"] == 0
+    assert info["workspace_bytes"] == 0
+    # the workspace covers the worst split of any lengths within the bounds:
+    # (largest block rows) x (blocks + CTAs) partial rows of 128 floats + one lse
+    prob, keep = _problem()
+    plan = B.attn_plan_replayable_host(prob, 152, keep)
+    info = B.attn_plan_info(plan)
+    rows = int(B.attn_plan_blocks(plan)[:, 3].max()) * (info["blocks"] + info["ctas"])
+    align = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert info["workspace_bytes"] == align(rows * 128 * 4) + align(rows * 4)
+    # a static plan never needs replanning
+    sprob, skeep = _problem()
+    with pytest.raises(B.AttnError) as e:
+        B.attn_plan_replan_host(B.attn_plan_host(sprob, 152, skeep), [100, 120])
+    assert e.value.status == B.ATTN_ERR_INVALID_ARG
+
+
 def _coverage_check(w, num_sms):
     prob, keep = _problem_of(w)
     return _check_plan(B.attn_plan_host(prob, num_sms, keep), w, num_sms)
