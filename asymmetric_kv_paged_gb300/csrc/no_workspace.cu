@@ -1,15 +1,15 @@
 // attn_run_paged_no_workspace: attn_run_paged with library-owned scratch.
 //
 // Some callers cannot allocate device memory at the point where they run
-// attention: code recording a CUDA graph (cudaMalloc is not allowed while a
-// stream is being captured), plugins that a host framework hands only tensor
-// pointers and no allocator, and serving loops that forbid allocation on the
-// hot path.  attn_run_paged needs a caller-provided workspace for split-KV
-// partials; this entry point instead uses one fixed-size array in device
-// global memory that belongs to the library.  The array is a file-scope
-// __device__ variable: every GPU that loads the library holds
-// ATTN_NO_WORKSPACE_MAX_BYTES of it until the process exits, and all calls
-// share it.
+// attention: plugins that a host framework hands tensor pointers but no
+// allocator (the framework owns every device byte through its own pool), and
+// serving loops that forbid cudaMalloc on the hot path (it can synchronise the
+// device and its latency is unbounded).  attn_run_paged needs a caller-provided
+// workspace for split-KV partials; this entry point instead uses one
+// fixed-size array in device global memory that belongs to the library.  The
+// array is a file-scope __device__ variable: every GPU that loads the library
+// holds ATTN_NO_WORKSPACE_MAX_BYTES of it until the process exits, and all
+// calls share it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,6 +27,8 @@ void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_scratch on `device`, looked up once per device with that
 // device current (in host code the symbol itself is only a host-side handle).
+// The address is cached for the life of the process; after cudaDeviceReset it
+// is stale (as are plans built before the reset).
 attn_status_t scratch_address(int device, void **addr) {
   if (device < 0 || device >= kMaxDevices) return ATTN_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mutex);
@@ -36,8 +38,9 @@ attn_status_t scratch_address(int device, void **addr) {
     if (prev != device && cudaSetDevice(device) != cudaSuccess) return ATTN_ERR_CUDA;
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-    if (prev != device) cudaSetDevice(prev);
-    if (e != cudaSuccess || !p) return ATTN_ERR_CUDA;
+    // put the caller's device back before anything else can fail
+    const cudaError_t back = prev != device ? cudaSetDevice(prev) : cudaSuccess;
+    if (e != cudaSuccess || !p || back != cudaSuccess) return ATTN_ERR_CUDA;
     g_scratch_addr[device] = p;
   }
   *addr = g_scratch_addr[device];

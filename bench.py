@@ -151,10 +151,22 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0: float, t1: float):
+        """Median SM clock and the throttle reasons seen inside [t0, t1].  When no
+        sample falls inside (a timed region shorter than the sampling period) the
+        in-region fields are null and `outside` summarises the samples taken while
+        this process ran the same workload around it."""
         inside = [p for t, p in self.samples if t0 <= t <= t1]
-        use = inside or [p for t, p in self.samples]
+        rec = self._stats(inside)
+        rec["samples_in_timed_region"] = len(inside)
+        rec["timed_region_ms"] = (t1 - t0) * 1e3
+        if not inside:
+            rec["outside"] = self._stats([p for _, p in self.samples])
+        return rec
+
+    @staticmethod
+    def _stats(use):
         if not use:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": None, "samples": 0}
 
         def num(x):
             try:
@@ -167,8 +179,7 @@ class ClockSampler:
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         reasons = sorted({n for p in use for n, v in zip(names, p[4:8]) if v.lower() == "active"})
         return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(use), "samples_in_timed_region": len(inside)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(use)}
 
 
 # ---------------------------------------------------------------- distributed

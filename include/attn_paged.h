@@ -231,17 +231,18 @@ attn_status_t attn_append_kv(attn_plan_t plan, const void *k_new, const void *v_
  *
  * The paper has no counterpart: this entry point exists for integration.
  * Some callers have no way to obtain the workspace attn_run_paged asks for:
- * code that runs while a stream is being captured into a CUDA graph (device
- * allocation is not permitted during capture), plugins that a host
- * framework hands tensor pointers but no allocator, and serving loops that
- * forbid allocation on the hot path.  This call takes the same arguments as
+ * plugins that a host framework hands tensor pointers but no allocator (the
+ * framework owns every device byte through its own memory pool), and serving
+ * loops that forbid cudaMalloc on the hot path, where it can synchronise the
+ * device and take unbounded time.  This call takes the same arguments as
  * attn_run_paged minus the workspace and uses instead one scratch array of
  * ATTN_NO_WORKSPACE_MAX_BYTES bytes in device global memory that the library
  * owns: every GPU that loads the library holds that array until the process
  * exits.  Nothing is allocated, here or later.
  *   - The first call on a device looks up the array's device address on that
  *     device (a host-side query, no allocation); make that first call before
- *     any stream capture.
+ *     any stream capture.  The address is kept for the life of the process
+ *     and is stale after cudaDeviceReset (as are plans made before it).
  *   - Plans whose workspace_bytes exceed ATTN_NO_WORKSPACE_MAX_BYTES are
  *     rejected with ATTN_ERR_WORKSPACE before anything is launched.
  *   - All calls share the one array, and it keeps whatever the last call left

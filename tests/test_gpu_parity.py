@@ -280,23 +280,64 @@ def test_evicted_pages_are_never_read(P, kv):
 
 # ---- full-size workloads, in the benchmark's launch configuration ----
 
-def sampled_rows(w, count, seed):
-    rng = np.random.default_rng(seed)
-    n = w.total_q * w.hq
-    rows = rng.choice(n, size=min(count, n), replace=False)
-    # always include the first and last rows (ragged edges)
-    return np.unique(np.concatenate([rows, [0, n - 1]]))
+def block_rows(w, blk):
+    """Flat output rows (token * Hq + head) of one plan block
+    {b, g, row0, nrows, ...}: block row r is token tok0 + r / G, head g*G + r % G."""
+    G = w.hq // w.hkv
+    b, g, row0, nrows = (int(x) for x in blk[:4])
+    r = row0 + np.arange(nrows)
+    tok = int(w.qo_indptr[b]) + r // G
+    return tok * w.hq + g * G + r % G
+
+
+def whole_blocks_to_check(w, plan, count=16):
+    """Indices of at least `count` whole row blocks: the first and last block of
+    every KV head, then blocks cut over several CTAs (their partials go through
+    the merge), the blocks just before and after each such cut first."""
+    from asymmetric_kv_paged_gb300 import binding as B
+    blocks = B.attn_plan_blocks(plan)
+    segs = B.attn_plan_segments(plan)
+    pick = []
+    for g in range(w.hkv):
+        idx = np.nonzero(blocks[:, 1] == g)[0]
+        if len(idx):
+            pick += [int(idx[0]), int(idx[-1])]
+    split = [int(i) for i in np.nonzero(blocks[:, 6] > 1)[0]]
+    # blocks whose first segment starts a CTA's share, i.e. sit right after a cut
+    starts = {int(segs[i, 1]) for i in range(len(segs))
+              if i == 0 or segs[i, 0] != segs[i - 1, 0]}
+    for i in split + sorted(starts):
+        if len(set(pick)) >= count:
+            break
+        pick.append(i)
+    rng = np.random.default_rng(5)
+    while len(set(pick)) < min(count, len(blocks)):
+        pick.append(int(rng.integers(len(blocks))))
+    return sorted(set(pick)), blocks
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", list(W.CONFIG_NAMES))
 def test_parity_named_config(name):
+    """Every output row of the decode, verify and SWA workloads at full size, and
+    at least 16 whole row blocks of the prefill chunk (first and last block of
+    every KV head and blocks split over several CTAs), each against the oracle."""
     w = W.named(name)
-    if name == "c1_tiny_decode":
+    if name != "c5_chunked_prefill":
         run_and_check(w)
-    else:
-        count = {"c5_chunked_prefill": 96}.get(name, 128)
-        run_and_check(w, rows=sampled_rows(w, count, seed=zlib.crc32(name.encode()) % 1000))
+        return
+    dw = _runner()(w)
+    dw.run()
+    torch.cuda.synchronize()
+    assert B_err(dw) == 0
+    picked, blocks = whole_blocks_to_check(w, dw.plan)
+    assert len(picked) >= 16
+    assert any(blocks[i, 6] > 1 for i in picked), "no split block among the checked ones"
+    rows = np.unique(np.concatenate([block_rows(w, blocks[i]) for i in picked]))
+    out = bf16_to_f64(dw.out).reshape(-1, W.DV)
+    lse = dw.lse.cpu().numpy().astype(np.float64).reshape(-1)
+    ref_out, ref_lse = oracle.attn_paged(w.host_arrays(), rows=rows)
+    check_rows(w, out[rows], lse[rows], ref_out, ref_lse, w.name)
 
 
 def test_batch_without_query_rows():

@@ -1,11 +1,12 @@
 """attn_run_paged_no_workspace: attention for callers that cannot allocate.
 
-Code that records a CUDA graph, plugins handed tensors but no allocator, and
-serving loops that forbid allocation cannot provide the workspace that
+Plugins that a host framework hands tensors but no allocator, and serving loops
+that forbid cudaMalloc on the hot path, cannot provide the workspace that
 attn_run_paged asks for.  This entry point runs the same kernels on a scratch
 array the library owns.  Here its output, on two calls in a row, is compared
 with attn_run_paged's output on a problem whose blocks are split over several
-CTAs (so the scratch really carries split-KV partials), within the parity
+CTAs (so the scratch really carries split-KV partials): the same kernels on the
+same plan must give the same bits, which also keeps it inside the parity
 tolerance of the other GPU tests.  This file is collected last so that a run
 stopping at its first failure has already run every other test; it also passes
 on its own in a fresh process.
@@ -49,6 +50,8 @@ def test_no_workspace_matches_workspace_path_twice():
         err = (got - ref).abs()
         assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
         assert (lse - ref_lse).abs().max().item() <= 2e-3 * max(1.0, ref_lse.abs().max().item())
+        # same kernels, same plan, same inputs: bit for bit the workspace path's result
+        assert torch.equal(got, ref) and torch.equal(lse, ref_lse)
     assert B.attn_get_device_error(dw.plan) == 0
 
 
