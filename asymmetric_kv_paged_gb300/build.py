@@ -19,9 +19,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "attn_tc.cu", "merge.cu", "replan.cu", "no_workspace.cu", "kv_append.cu",
+SOURCES = ["api.cu", "attn_tc.cu", "attn_prefill.cu", "merge.cu", "replan.cu", "no_workspace.cu", "kv_append.cu",
            "tc_selftest.cu", "planner.cpp"]
-HEADERS = ["plan.hpp", "replan.hpp", "kernels.hpp", "tc_common.cuh"]
+HEADERS = ["plan.hpp", "replan.hpp", "kernels.hpp", "tc_common.cuh", "e4m3.cuh"]
 
 
 def build_dir() -> str:

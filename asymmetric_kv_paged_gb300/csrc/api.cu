@@ -115,7 +115,7 @@ attn_status_t upload(attn_plan_s *p) {
     e = cudaMemcpy(p->dev.seq_bounds, hp.seq_lens.data(), hp.seq_lens.size() * sizeof(int32_t),
                    cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(p->dev.err, 0, e_bytes);
-  if (e == cudaSuccess) e = akp::prepare_attn_tc(hp);
+  if (e == cudaSuccess) e = hp.prefill ? akp::prepare_attn_prefill(hp) : akp::prepare_attn_tc(hp);
   if (e != cudaSuccess) {
     free_device(p);
     return ATTN_ERR_CUDA;
@@ -251,7 +251,7 @@ static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const
   a.err = plan->dev.err;
 
   akp::TmaMaps maps{};
-  if ((phases & 1) && hp.use_tma) {
+  if ((phases & 1) && hp.use_tma && !hp.prefill) {
     if ((reinterpret_cast<uintptr_t>(k_cache) & 15) || (reinterpret_cast<uintptr_t>(v_cache) & 15))
       return ATTN_ERR_INVALID_ARG;
     const int64_t slots = (int64_t)pr.num_pages * pr.page_size;
@@ -279,9 +279,14 @@ static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const
     r.num_ctas = hp.num_ctas;
     r.group = hp.group;
     r.window = pr.window;
+    r.key_tile = hp.key_tile;
     if (akp::launch_replan(r, st) != cudaSuccess) return ATTN_ERR_CUDA;
   }
-  if ((phases & 1) && akp::launch_attn_tc(hp, a, maps, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (phases & 1) {
+    const cudaError_t le = hp.prefill ? akp::launch_attn_prefill(hp, a, st)
+                                      : akp::launch_attn_tc(hp, a, maps, st);
+    if (le != cudaSuccess) return ATTN_ERR_CUDA;
+  }
   if ((phases & 2) && akp::launch_merge(hp, a, st) != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
@@ -341,7 +346,7 @@ attn_status_t attn_plan_info(attn_plan_t plan, int32_t info[8]) {
   info[1] = (int32_t)hp.segs.size();
   info[2] = hp.num_ctas;
   info[3] = hp.block_rows;
-  info[4] = akp::kKeyTile;
+  info[4] = hp.key_tile;
   info[5] = hp.multi_split_blocks;
   info[6] = (int32_t)(hp.workspace_bytes & 0x7FFFFFFF);
   info[7] = (int32_t)(hp.workspace_bytes >> 31);

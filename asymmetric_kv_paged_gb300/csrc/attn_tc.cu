@@ -15,7 +15,7 @@
 //   warps 0-3  softmax + epilogue: MMA row p lives in TMEM lane p (M=128) or
 //              in lane 32*(p/16) + p%16 (M=64), and that lane's thread owns it;
 //   warps 4-7  converters: stage Q per block; turn raw FP8 K/V tiles into
-//              exact fp16 operand tiles; zero V rows of keys outside the
+//              exact bf16 operand tiles; zero V rows of keys outside the
 //              block's range on edge tiles (unused slots may hold NaN:
 //              sammysun0711/sglang PR #35, FlyPA V-tail masking); or, for
 //              page sizes TMA cannot tile, gather K/V rows themselves;
@@ -29,13 +29,13 @@
 // Every wait is bounded in time; a broken invariant ends the kernel with bit 1
 // of the plan's error word set instead of hanging the GPU.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include <cmath>
 #include <cstdint>
 #include <type_traits>
 
+#include "e4m3.cuh"
 #include "kernels.hpp"
 #include "tc_common.cuh"
 
@@ -51,7 +51,7 @@ constexpr int kRawK = kN * kDqk;             // raw E4M3 K rows: 12 KB
 constexpr int kRawBytes = kRawK + kN * kDv;  // + raw V rows: 20 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 128;             // O: 128 fp32 columns
-constexpr uint32_t kTmemP = 256;             // P double buffer: 2 x 32 columns (bf16/fp16 pairs)
+constexpr uint32_t kTmemP = 256;             // P double buffer: 2 x 32 columns (bf16 pairs)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;    // base-2 growth allowed before O is rescaled
@@ -159,40 +159,9 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ uint32_t cvt_pair(float lo, float hi, bool half) {
-  if (half) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-  }
+__device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// 16 E4M3 codes -> 16 fp16 values (exact: every E4M3 value is an fp16
-// value), as two 16-byte chunks.  One cvt.rn.f16x2.e4m3x2 turns the two
-// codes of a 16-bit half-word into an fp16 pair, low byte to low half.
-__device__ __forceinline__ void e4m3x16_to_f16(const uint4 raw, uint4 &lo, uint4 &hi) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t h[8];
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    asm("{\n .reg .b16 l, u;\n mov.b32 {l, u}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n"
-        " cvt.rn.f16x2.e4m3x2 %1, u;\n}\n"
-        : "=r"(h[2 * q]), "=r"(h[2 * q + 1])
-        : "r"(w[q]));
-  lo = make_uint4(h[0], h[1], h[2], h[3]);
-  hi = make_uint4(h[4], h[5], h[6], h[7]);
-}
-
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&w[q]);
-    __half2 h = __float22half2_rn(__bfloat1622float2(b));
-    w[q] = *reinterpret_cast<uint32_t *>(&h);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
@@ -222,7 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kQBlock = Lay::kQBlock;
   constexpr int NS = Lay::kOpStages;
   constexpr int NT = Lay::kTmaStages;
-  constexpr bool kHalf = FP8;  // operand type: fp16 for FP8 caches, bf16 otherwise
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   __shared__ Bars bars;
@@ -430,8 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int idx = ct + (i0 + u) * 128;
           const int p = idx / 24;
           const int ch = idx % 24;
-          const uint4 w = kHalf ? bf16x8_to_f16x8(v[u]) : v[u];
-          *reinterpret_cast<uint4 *>(qs + (ch >> 3) * kQBlock + tc::sw128_offset(p, ch & 7)) = w;
+          *reinterpret_cast<uint4 *>(qs + (ch >> 3) * kQBlock + tc::sw128_offset(p, ch & 7)) = v[u];
         }
       }
       tc::fence_proxy_async_smem();
@@ -478,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kk = c / kKch, c16 = 2 * (c % kKch);
           const int j = key0 + kk;
           uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-          if (j >= bd.klo && j < bd.khi) e4m3x16_to_f16(bk[u], lo, hi);
+          if (j >= bd.klo && j < bd.khi) e4m3x16_to_bf16(bk[u], lo, hi);
           *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
           *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
                                      tc::sw128_offset(kk, (c16 + 1) & 7)) = hi;
@@ -494,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kk = c / kVch, c16 = 2 * (c % kVch);
           const int j = key0 + kk;
           uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-          if (j >= bd.klo && j < bd.khi) e4m3x16_to_f16(bv[u], lo, hi);
+          if (j >= bd.klo && j < bd.khi) e4m3x16_to_bf16(bv[u], lo, hi);
           *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
           *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
                                      tc::sw128_offset(kk, (c16 + 1) & 7)) = hi;
@@ -575,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *dst = op + (is_k ? 0 : kOpK);
         if (FP8) {
           uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-          if (keep) e4m3x16_to_f16(buf[u], lo, hi);
+          if (keep) e4m3x16_to_bf16(buf[u], lo, hi);
           const int c16 = 2 * ch;
           *reinterpret_cast<uint4 *>(dst + (c16 >> 3) * kBlk + tc::sw128_offset(kk, c16 & 7)) = lo;
           *reinterpret_cast<uint4 *>(dst + ((c16 + 1) >> 3) * kBlk +
@@ -596,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // as long as the tensor pipe takes to accept it, so with one issuer P.V of
     // tile k would queue behind the whole Q.K^T of tile k+1.
     if ((tid & 31) == 0) {
-      const uint32_t id_s = tc::idesc_f16(kHalf ? 0 : 1, 0, 0, kRows, kN);
+      const uint32_t id_s = tc::idesc_f16(1, 0, 0, kRows, kN);
       Cursor cs;
       cs.init(a.segs, a.blocks, seg_begin, seg_end);
       // BF16 + TMA: interior tiles are consumed straight off the TMA barrier;
@@ -644,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 10) {
     // ------------------------------------------------------------ O += P.V issuer
     if ((tid & 31) == 0) {
-      const uint32_t id_pv = tc::idesc_f16(kHalf ? 0 : 1, 0, 1, kRows, kDv);
+      const uint32_t id_pv = tc::idesc_f16(1, 0, 1, kRows, kDv);
       Cursor cp;
       cp.init(a.segs, a.blocks, seg_begin, seg_end);
       for (int kp = 0; kp < total; ++kp, cp.next()) {
@@ -790,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p0 = ex2(fmaf(x0, sc, neg_m));
           const float p1 = ex2(fmaf(x1, sc, neg_m));
           rs[(j >> 1) & 3] += p0 + p1;
-          pk[j / 2] = cvt_pair(p0, p1, kHalf);
+          pk[j / 2] = cvt_pair(p0, p1);
         }
         tc::tmem_st8(pcol + 8 * (g0 + c), pk);
       };
@@ -931,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                   w[e] = cvt_pair(__uint_as_float(o[8 * q + 2 * e]) * scale_o,
-                                  __uint_as_float(o[8 * q + 2 * e + 1]) * scale_o, false);
+                                  __uint_as_float(o[8 * q + 2 * e + 1]) * scale_o);
                 dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
               }
             } else {

@@ -38,6 +38,9 @@ cudaError_t launch_attn_tc(const HostPlan &hp, const RunArgs &a, const TmaMaps &
                            cudaStream_t stream);
 // One-time per-device kernel attributes (dynamic shared memory limits).
 cudaError_t prepare_attn_tc(const HostPlan &hp);
+// Prefill plans (hp.prefill: 256-row blocks, 128-key tiles): attn_prefill.cu.
+cudaError_t launch_attn_prefill(const HostPlan &hp, const RunArgs &a, cudaStream_t stream);
+cudaError_t prepare_attn_prefill(const HostPlan &hp);
 // Whether K/V tiles of this page size can be loaded as TMA boxes.
 bool tc_tma_page_size(int32_t page_size, int32_t num_pages);
 // Device planner of replayable plans (replan.cu): rewrites the work list

@@ -11,12 +11,14 @@ namespace akp {
 
 constexpr int kDqk = 192;       // query/key head dim
 constexpr int kDv = 128;        // value head dim
-constexpr int kKeyTile = 64;    // keys per pipeline tile
+constexpr int kKeyTile = 64;    // keys per pipeline tile (decode / verify kernel)
+constexpr int kPrefillKeyTile = 128;   // keys per tile of the prefill kernel
 
 // Query rows per row block.  A block packs up to block_rows query rows of one
 // (request, KV head): row r <-> (token r / G, head g*G + r % G); decode blocks
-// hold G rows, verify blocks n*G, prefill blocks 128.  block_rows is 64 (M=64
-// MMAs) when no (request, KV head) has more than 64 query rows, else 128.
+// hold G rows, verify blocks n*G.  block_rows is 64 (M=64 MMAs) when no
+// (request, KV head) has more than 64 query rows, 128 when none has more than
+// 128, else 256: the prefill kernel's two 128-row Q tiles over 128-key tiles.
 
 // One row block: rows [row0, row0 + nrows) of (b, g).  Keys [klo, khi) are
 // the union of what its rows can see.
@@ -43,7 +45,9 @@ struct HostPlan {
   attn_problem_t prob{};
   std::vector<int32_t> qo_indptr, seq_lens;
   int32_t group = 1;             // G = Hq / Hkv
-  int32_t block_rows = 128;      // 64 or 128 (the MMA M)
+  int32_t block_rows = 128;      // 64 or 128 (the MMA M), or 256 (prefill kernel)
+  int32_t key_tile = kKeyTile;   // keys per tile: 64, or 128 for the prefill kernel
+  bool prefill = false;          // block_rows == 256: attn_prefill.cu runs the plan
   int32_t num_sms = 0, num_ctas = 0, threads = 0;
   std::vector<BlockDesc> blocks;
   std::vector<SegDesc> segs;

@@ -58,8 +58,11 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   // M = 64 halves the Q and P tiles, so one more K/V stage fits (and Q can be
   // double-buffered); for blocks of up to 64 rows that beats M = 128's second
   // row copy, measured on 8- and 64-row blocks.
-  hp.block_rows = max_rows <= 64 ? 64 : 128;
+  hp.block_rows = max_rows <= 64 ? 64 : max_rows <= 128 ? 128 : 256;
+  hp.prefill = hp.block_rows == 256;
+  hp.key_tile = hp.prefill ? kPrefillKeyTile : kKeyTile;
   const int32_t rows_per_block = hp.block_rows;
+  const int32_t tile = hp.key_tile;
   const int32_t G = hp.group;
 
   // Row blocks.
@@ -87,7 +90,7 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
         if (p->window > 0) lo = std::max<int64_t>(0, i_first - p->window + 1);
         bd.klo = (int32_t)lo;
         bd.khi = (int32_t)(i_last + 1);
-        total_tiles += (bd.khi - 1) / kKeyTile - bd.klo / kKeyTile + 1;
+        total_tiles += (bd.khi - 1) / tile - bd.klo / tile + 1;
         hp.blocks.push_back(bd);
       }
     }
@@ -107,8 +110,8 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
     int64_t room = 0, target = 0, slack = 0;
     for (int64_t bi = 0; bi < nb; ++bi) {
       BlockDesc &bd = hp.blocks[bi];
-      int32_t t0 = bd.klo / kKeyTile;
-      const int32_t tend = (bd.khi - 1) / kKeyTile + 1;
+      int32_t t0 = bd.klo / tile;
+      const int32_t tend = (bd.khi - 1) / tile + 1;
       int32_t split = 0;
       while (t0 < tend) {
         if (room <= 0) {
@@ -124,7 +127,7 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
         // place: a fresh CTA takes it whole, a CTA it does not fit in leaves it
         // to the next one.  For such a block a split's extra segment and merge
         // cost more than the room left unused.
-        const bool whole = t0 == bd.klo / kKeyTile && left <= kWholeBlockTiles &&
+        const bool whole = t0 == bd.klo / tile && left <= kWholeBlockTiles &&
                            left <= 2 * target && nb - bi <= (int64_t)num_sms - cta - 1;
         if (whole && room < target && left > room + slack) {
           room = 0;
@@ -176,7 +179,7 @@ attn_status_t build_replayable_plan(const attn_problem_t *p, int32_t num_sms, Ho
   int64_t max_tiles = 0;
   int32_t max_rows = 0;
   for (const BlockDesc &bd : hp.blocks) {
-    max_tiles += (bd.khi - 1) / kKeyTile + 1;
+    max_tiles += (bd.khi - 1) / hp.key_tile + 1;
     max_rows = std::max(max_rows, bd.nrows);
   }
   if (max_tiles >= INT32_MAX / 2) return ATTN_ERR_UNSUPPORTED;
@@ -215,7 +218,7 @@ int32_t replan_host(HostPlan *hp, const int32_t *seq_lens) {
     bd.L = L;
     bd.klo = klo;
     bd.khi = khi;
-    start[bi + 1] = start[bi] + block_tile_count(klo, khi);
+    start[bi + 1] = start[bi] + block_tile_count(klo, khi, hp->key_tile);
   }
   const int64_t T = start[nb];
   const int64_t ctas = std::min<int64_t>(T, hp->num_ctas);
@@ -226,8 +229,8 @@ int32_t replan_host(HostPlan *hp, const int32_t *seq_lens) {
     if (c < ctas) {
       const int64_t a = share_begin(c, T, ctas), e = share_begin(c + 1, T, ctas);
       for (int32_t bi = block_at(start.data(), nb, a); bi < nb && start[bi] < e; ++bi) {
-        hp->segs.push_back(
-            share_segment(bi, hp->blocks[bi], start[bi], start[bi + 1], a, e, c, T, ctas));
+        hp->segs.push_back(share_segment(bi, hp->blocks[bi], start[bi], start[bi + 1], a, e, c, T,
+                                         ctas, hp->key_tile));
         hp->seg_cta.push_back(c);
       }
     }

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kReplanThreads, 1) replan_kernel(const ReplanA
     bd.L = L;
     bd.klo = klo;
     bd.khi = khi;
-    r.tile_start[bi] = block_tile_count(klo, khi);
+    r.tile_start[bi] = block_tile_count(klo, khi, r.key_tile);
   }
   __syncthreads();
   cta_exclusive_scan(r.tile_start, r.nb);
@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(kReplanThreads, 1) replan_kernel(const ReplanA
     for (int32_t bi = block_at(r.tile_start, r.nb, a); bi < r.nb; ++bi) {
       const int64_t gs = r.tile_start[bi];
       if (gs >= e) break;
-      r.segs[s++] = share_segment(bi, r.blocks[bi], gs, r.tile_start[bi + 1], a, e, c, T, ctas);
+      r.segs[s++] = share_segment(bi, r.blocks[bi], gs, r.tile_start[bi + 1], a, e, c, T, ctas,
+                                   r.key_tile);
     }
   }
 

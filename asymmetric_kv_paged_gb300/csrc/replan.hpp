@@ -36,9 +36,9 @@ AKP_HD void block_keys(const BlockDesc &bd, int32_t L, int32_t group, int32_t wi
   *khi = (int32_t)(i_last + 1);
 }
 
-// Key tiles touched by keys [klo, khi) (klo < khi).
-AKP_HD int32_t block_tile_count(int32_t klo, int32_t khi) {
-  return (khi - 1) / kKeyTile - klo / kKeyTile + 1;
+// Key tiles of `tile` keys touched by keys [klo, khi) (klo < khi).
+AKP_HD int32_t block_tile_count(int32_t klo, int32_t khi, int32_t tile) {
+  return (khi - 1) / tile - klo / tile + 1;
 }
 
 // First global tile position of CTA c's share (c = ctas gives T).
@@ -67,8 +67,8 @@ AKP_HD int32_t block_at(const int32_t *start, int32_t nb, int64_t x) {
 // Segment of block bi inside CTA c's share [a, e), with the block at global
 // positions [gs, ge).
 AKP_HD SegDesc share_segment(int32_t bi, const BlockDesc &bd, int64_t gs, int64_t ge, int64_t a,
-                             int64_t e, int32_t c, int64_t T, int64_t ctas) {
-  const int32_t tb = bd.klo / kKeyTile;
+                             int64_t e, int32_t c, int64_t T, int64_t ctas, int32_t tile) {
+  const int32_t tb = bd.klo / tile;
   const int64_t lo = a > gs ? a : gs;
   const int64_t hi = e < ge ? e : ge;
   SegDesc s;
@@ -94,7 +94,7 @@ struct ReplanArgs {
   const int32_t *seq_lens;     // [B] lengths of this run (caller's device array)
   const int32_t *seq_bounds;   // [B] upper bounds the plan was built for
   int32_t *err;                // device error word (bit 4: a length out of bounds)
-  int32_t nb, num_ctas, group, window;
+  int32_t nb, num_ctas, group, window, key_tile;
 };
 
 }  // namespace akp

@@ -85,11 +85,19 @@ def peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def kernel_of(workload: str) -> str:
+    """The attention kernel a named workload's plan launches: the prefill kernel
+    for blocks of more than 128 query rows, the split-KV kernel otherwise."""
+    return "attn_prefill" if workload.startswith("c5") else "attn_tc"
+
+
 def split_kernel_traffic(workload: str):
-    """DRAM bytes per launch of the attention kernel from a committed ncu summary,
-    when that summary was taken on the kernel source as it is now (else None)."""
-    path = os.path.join(ROOT, "profiles", f"attn_tc_{workload}.md")
-    src = os.path.join(ROOT, "asymmetric_kv_paged_gb300", "csrc", "attn_tc.cu")
+    """DRAM bytes per launch of the workload's attention kernel from a committed ncu
+    summary, when that summary was taken on the kernel source as it is now (else
+    None)."""
+    kern = kernel_of(workload)
+    path = os.path.join(ROOT, "profiles", f"{kern}_{workload}.md")
+    src = os.path.join(ROOT, "asymmetric_kv_paged_gb300", "csrc", f"{kern}.cu")
     if not os.path.exists(path):
         return None
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -265,47 +273,132 @@ def time_workload(dw, steps: int, warmup: int, world: int, flush_l2: bool = Fals
                 attn_ms=step, t0=t0, t1=t1, launches=steps * (2 if has_merge else 1))
 
 
-def e2e_measure(dw, steps: int, warmup: int, world: int):
-    """Per step: q, page table, seq_lens, qo_indptr copied host->device from pinned
-    buffers, attn_run_paged, out copied device->host.  The K/V cache is state and
-    stays resident."""
-    import torch
-    w = dw.w
-    stream = torch.cuda.current_stream()
-    h_q = torch.from_numpy(w.q).view(torch.bfloat16).pin_memory()
-    h_pt = torch.from_numpy(w.page_table).pin_memory()
-    h_sl = torch.from_numpy(w.seq_lens).pin_memory()
-    h_qo = torch.from_numpy(w.qo_indptr).pin_memory()
-    h_out = torch.empty(dw.out.shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_sl, h_qo))
-    d2h = h_out.numel() * h_out.element_size()
+def grown_workload(w, extra: int):
+    """A copy of decode workload `w` whose requests can grow by `extra` tokens: the
+    page table gains fresh pages from the pool's unused ones, and seq_lens become
+    the upper bounds of a replayable plan."""
+    import copy
+    P = w.page_size
+    L = w.seq_lens.astype(np.int64)
+    have = (L + P - 1) // P
+    need = (L + extra + P - 1) // P
+    used = set(int(x) for x in np.unique(w.page_table))
+    free = [p for p in range(w.num_pages) if p not in used]
+    assert len(free) > int((need - have).sum()), "pool too small to grow the batch"
+    # columns past a request's pages point at an unused (NaN) page, as in the workload
+    pt = np.full((w.batch, int(need.max())), free.pop(), np.int32)
+    pt[:, :w.page_table.shape[1]] = w.page_table
+    it = iter(free)
+    for b in range(w.batch):
+        for j in range(int(have[b]), int(need[b])):
+            pt[b, j] = next(it)
+    g = copy.copy(w)
+    g.page_table = pt
+    g.seq_lens = (L + extra).astype(np.int32)
+    return g
 
-    def step():
+
+def e2e_measure(w, steps: int, warmup: int, world: int):
+    """One decode serving step per timed step, through the C ABI from pinned host
+    memory: every request grows by one token per step.  Per step: q, the new
+    token's K/V rows, the lengths, qo_indptr and the page table are copied in,
+    attn_append_kv writes the new K/V into the paged cache, attn_run_paged runs on
+    a replayable plan (lengths read on the device: planner kernel, attention,
+    merge), and the output is copied back.  The K/V cache is state and stays
+    resident.  Also reported: the same copies around a static plan whose lengths
+    never change (`static`), and the host cost of attn_plan for this batch."""
+    import torch
+    from asymmetric_kv_paged_gb300 import binding as B
+    from asymmetric_kv_paged_gb300.runner import DeviceWorkload
+    total = warmup + steps
+    g = grown_workload(w, total)
+    dw = DeviceWorkload(g, device=torch.cuda.current_device(), with_lse=False, replayable=True)
+    stream = torch.cuda.current_stream()
+    L0 = w.seq_lens.astype(np.int64)
+    rng = np.random.default_rng(7)
+    h_q = torch.from_numpy(w.q).view(torch.bfloat16).pin_memory()
+    h_kn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, DQK), dtype=np.float32)).to(
+        torch.bfloat16).pin_memory()
+    h_vn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, DV), dtype=np.float32)).to(
+        torch.bfloat16).pin_memory()
+    h_pt = torch.from_numpy(g.page_table).pin_memory()
+    h_qo = torch.from_numpy(w.qo_indptr).pin_memory()
+    h_sl = torch.from_numpy(np.stack([(L0 + s).astype(np.int32) for s in range(total)])).pin_memory()
+    h_out = torch.empty(dw.out.shape, dtype=torch.bfloat16).pin_memory()
+    d_kn = torch.empty(h_kn.shape, dtype=torch.bfloat16, device=dw.q.device)
+    d_vn = torch.empty(h_vn.shape, dtype=torch.bfloat16, device=dw.q.device)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_pt, h_qo)) + h_sl[0].numel() * 4
+    d2h = h_out.numel() * h_out.element_size()
+    ks, vs = (w.k_scale, w.v_scale) if w.kv_dtype == "fp8" else (1.0, 1.0)
+
+    def step(s):
         dw.q.copy_(h_q, non_blocking=True)
-        dw.page_table.copy_(h_pt, non_blocking=True)
-        dw.seq_lens.copy_(h_sl, non_blocking=True)
+        d_kn.copy_(h_kn, non_blocking=True)
+        d_vn.copy_(h_vn, non_blocking=True)
+        dw.seq_lens.copy_(h_sl[s], non_blocking=True)
         dw.qo_indptr.copy_(h_qo, non_blocking=True)
+        dw.page_table.copy_(h_pt, non_blocking=True)
+        B.attn_append_kv(dw.plan, d_kn, d_vn, dw.k_cache, dw.v_cache, dw.page_table, dw.seq_lens,
+                         dw.qo_indptr, ks, vs, stream)
         dw.run(stream)
         h_out.copy_(dw.out, non_blocking=True)
 
-    for _ in range(warmup):
-        step()
+    for s in range(warmup):
+        step(s)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     start.record(stream)
-    for _ in range(steps):
-        step()
+    for s in range(warmup, total):
+        step(s)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    # plan cost (host planning + upload), once per batch shape; reported apart
+    assert B.attn_get_device_error(dw.plan) == 0
+    grown_bytes = [algorithmic_bytes(_with_lens(w, L0 + s)) for s in range(warmup, total)]
+    ms = start.elapsed_time(end) / steps
+    del dw
+    torch.cuda.empty_cache()
+
+    # the static-plan figure: same batch, lengths fixed, no append
+    sw = DeviceWorkload(w, device=torch.cuda.current_device(), with_lse=False)
+    h_pt0 = torch.from_numpy(w.page_table).pin_memory()
+    h_sl0 = torch.from_numpy(w.seq_lens).pin_memory()
+
+    def static_step():
+        sw.q.copy_(h_q, non_blocking=True)
+        sw.page_table.copy_(h_pt0, non_blocking=True)
+        sw.seq_lens.copy_(h_sl0, non_blocking=True)
+        sw.qo_indptr.copy_(h_qo, non_blocking=True)
+        sw.run(stream)
+        h_out.copy_(sw.out, non_blocking=True)
+
+    for _ in range(warmup):
+        static_step()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        static_step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    static_ms = start.elapsed_time(end) / steps
     t = time.time()
     for _ in range(3):
-        dw.make_plan().destroy()
+        sw.make_plan().destroy()
     plan_ms = (time.time() - t) / 3 * 1e3
-    return dict(ms=start.elapsed_time(end) / steps, h2d=h2d, d2h=d2h, plan_ms=plan_ms)
+    del sw
+    torch.cuda.empty_cache()
+    return dict(ms=ms, h2d=h2d, d2h=d2h, bytes=float(np.mean(grown_bytes)), static_ms=static_ms,
+                static_h2d=sum(t.numel() * t.element_size() for t in (h_q, h_pt0, h_sl0, h_qo)),
+                plan_ms=plan_ms)
+
+
+def _with_lens(w, lens):
+    import copy
+    g = copy.copy(w)
+    g.seq_lens = np.asarray(lens, dtype=np.int32)
+    return g
 
 
 def cpu_baseline(w, budget_s: float = 12.0):
@@ -400,7 +493,8 @@ def measure_extra(name: str, pk: dict, steps: int, warmup: int, world: int):
                "ms_per_step": r["attn_ms"], "roofline": {"bound": "tensor", "achieved": achieved,
                                                            "peak": peak, "unit": "TFLOP/s",
                                                            "frac": achieved / peak,
-                                                           "traffic": split_kernel_traffic(name)}}
+                                                           "traffic": split_kernel_traffic(name),
+                                                           "kernel": kernel_of(name) + "_kernel"}}
     else:
         achieved = nbytes / (r["split_ms"] * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
@@ -408,7 +502,8 @@ def measure_extra(name: str, pk: dict, steps: int, warmup: int, world: int):
                "ms_per_step": r["attn_ms"], "roofline": {"bound": "hbm", "achieved": achieved,
                                                            "peak": peak, "unit": "GB/s",
                                                            "frac": achieved / peak,
-                                                           "traffic": split_kernel_traffic(name)}}
+                                                           "traffic": split_kernel_traffic(name),
+                                                           "kernel": kernel_of(name) + "_kernel"}}
     out.update(split_ms=r["split_ms"], merge_ms=r["merge_ms"], algorithmic_bytes=nbytes,
                flops=flops, l2="flushed between steps" if small else "inputs larger than L2")
     del dw
@@ -479,10 +574,12 @@ def run_ours(args):
         sampler.stop()
     step_ms = max_over_ranks(r["step_ms"], world)
     split_ms = max_over_ranks(r["split_ms"], world)
-    e2e = e2e_measure(dw, max(10, args.steps // 4), 3, world)
-    e2e_ms = max_over_ranks(e2e["ms"], world)
     assert binding.attn_get_device_error(dw.plan) == 0
-
+    del dw
+    torch.cuda.empty_cache()
+    e2e = None if args.no_e2e else e2e_measure(w, max(10, args.steps // 4), 3, world)
+    e2e_ms = max_over_ranks(e2e["ms"], world) if e2e else None
+    static_ms = max_over_ranks(e2e["static_ms"], world) if e2e else None
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": nbytes * world / (step_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -494,9 +591,17 @@ def run_ours(args):
                      "frac": achieved / pk["hbm_gbs"], "traffic": split_kernel_traffic(args.workload),
                      "kernel": "attn_tc_kernel", "kernel_ms": split_ms, "merge_ms": r["merge_ms"],
                      "peak_source": f"{pk['source']} (hbm_gbs)"},
-        "e2e": {"value": nbytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": None if e2e is None else {
+                "value": e2e["bytes"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": e2e_ms, "plan_ms_per_batch_shape": e2e["plan_ms"]},
+                "ms_per_step": e2e_ms,
+                "step": "serving decode step: every length +1 per step; KV append + "
+                        "replayable-plan attention (planner kernel, attention, merge)",
+                "static": {"value": nbytes * world / (static_ms * 1e-3) / 1e9, "unit": "GB/s",
+                           "ms_per_step": static_ms, "h2d_bytes_per_step": e2e["static_h2d"],
+                           "d2h_bytes_per_step": e2e["d2h"],
+                           "step": "static plan, lengths fixed, no append"},
+                "plan_ms_per_batch_shape": e2e["plan_ms"]},
         "gpu_launches": r["launches"],
         "clocks": clocks,
     }
@@ -582,6 +687,7 @@ def main():
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end serving measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -162,8 +162,10 @@ attn_status_t attn_plan_replayable(const attn_problem_t *bounds, int device, att
  *   workspace    device scratch of at least workspace_bytes (may be NULL when
  *                the plan reported 0).  Its contents need no initialisation.
  * Slots of the caches that no query can see are never read, so they may hold
- * anything (NaN included).  Queries are read as bf16; with an FP8 cache the
- * products are formed in fp16 (|q| must stay below 65504).
+ * anything (NaN included).  Queries are used as the bf16 values given, for
+ * either cache type: E4M3 elements are widened exactly to bf16 and every
+ * product is bf16 x bf16 with fp32 accumulation.  The E4M3 NaN codes (0x7F,
+ * 0xFF) in a visible slot are not propagated (they read as +-480).
  * Runs of one plan must be ordered on one stream (they share the plan's
  * device error word); different plans are independent.
  * Errors: INVALID_ARG, WORKSPACE, CUDA (launch errors; nothing is waited for).

@@ -200,7 +200,7 @@ def test_named_configs_schedule_shape():
         ("decode", [1024 + 37 * i for i in range(32)], [1] * 32, 16, 2, 128, 0, 64),
         ("verify", [46008] * 4, [8] * 4, 16, 2, 128, 0, 64),
         ("swa", [8192] * 64, [1, 8] * 32, 16, 2, 128, 128, 64),
-        ("prefill", [30096], [4096], 64, 4, 128, 0, 128),
+        ("prefill", [30096], [4096], 64, 4, 128, 0, 256),
     ]:
         prob, keep = B.make_problem(batch=len(seq), num_q_heads=hq, num_kv_heads=hkv,
                                     page_size=P, num_pages=9375,

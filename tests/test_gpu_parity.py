@@ -162,6 +162,63 @@ def test_k_path_index_exact(P, kv):
         assert np.all(np.abs(got[:, h] - expect) < 1e-3), f"head {h}"
 
 
+@pytest.mark.parametrize("q_std", [1e5, 1e-6], ids=["q_1e5", "q_1e-6"])
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_fp8_keeps_q_exact(q_std, mode):
+    """With FP8 caches Q stays bf16: queries far outside fp16's range (|q| ~ 1e5)
+    or deep in its subnormals (|q| ~ 1e-6), with the softmax scale set so the
+    scores stay of order one, still match the oracle (the pages keep Q.K in
+    16-bit: model card "Things that were measured and did not help")."""
+    seq, n, hq, hkv = ([1500, 333], [8, 1], 16, 2) if mode == "decode" else ([700], [200], 32, 2)
+    w = W.make_workload(31 if mode == "decode" else 32, seq, n, hq=hq, hkv=hkv, page_size=16,
+                        kv_dtype="fp8", q_std=q_std,
+                        softmax_scale=1.0 / (q_std * np.sqrt(W.DQK)), name=f"fp8_q{q_std:g}")
+    run_and_check(w)
+
+
+@pytest.mark.parametrize("P", [1, 128])
+def test_fp8_every_code_exact(P):
+    """Every finite E4M3 code through both load paths.  V: window 1 with n = L, so
+    row t returns V row t bit for bit (the code's exact bf16 value, a zero's sign
+    aside).  K: one-hot
+    queries read one K column each, and lse / scale recovers that element."""
+    L, hq, hkv = 300, 8, 2
+    G = hq // hkv
+    w = W.make_workload(41, [L], [L], hq=hq, hkv=hkv, page_size=P, window=1, kv_dtype="fp8")
+    w.k_scale = w.v_scale = 1.0
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    t = np.arange(L)
+    slots = w.page_table[0, t // P].astype(np.int64) * P + t % P
+    vc = w.v_cache.reshape(-1, hkv, W.DV).copy()
+    kc = w.k_cache.reshape(-1, hkv, W.DQK).copy()
+    for g in range(hkv):
+        vc[slots, g] = finite[(t[:, None] * W.DV + np.arange(W.DV) + 97 * g) % finite.size]
+        kc[slots, g, :G] = finite[(t[:, None] * G + np.arange(G) + 31 * g) % finite.size]
+    w.v_cache = vc.reshape(w.v_cache.shape)
+    w.k_cache = kc.reshape(w.k_cache.shape)
+    q = np.zeros((L, hq, W.DQK), np.float32)
+    for h in range(hq):
+        q[:, h, h % G] = 1.0
+    w.q = W.bf16_bits(q)
+    dw = _runner()(w)
+    dw.run()
+    torch.cuda.synchronize()
+    assert B_err(dw) == 0
+    got_v = dw.out.view(torch.int16).cpu().numpy().view(np.uint16)
+    as_bf16 = lambda codes: torch.from_numpy(np.ascontiguousarray(codes)).view(
+        torch.float8_e4m3fn).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got_k = dw.lse.cpu().numpy().astype(np.float64) / w.softmax_scale
+    # -0 comes out as +0: the accumulator adds the zero products of the tile's
+    # other (masked) keys, so only the sign of a zero may differ
+    plus0 = lambda bits: np.where(bits == 0x8000, 0, bits)  # noqa: E731
+    for h in range(hq):
+        g = h // G
+        assert np.array_equal(plus0(got_v[:, h]), plus0(as_bf16(vc[slots, g]))), f"V, head {h}"
+        expect = torch.from_numpy(kc[slots, g, h % G].copy()).view(torch.float8_e4m3fn).double().numpy()
+        assert np.all(np.abs(got_k[:, h] - expect) <= 1e-5 * np.maximum(1.0, np.abs(expect))), \
+            f"K, head {h}"
+
+
 def test_repeat_runs_bit_identical():
     w = W.make_workload(8, [3000, 1200], [8, 1], hq=16, hkv=2, page_size=128, sinks=True)
     dw = _runner()(w)
