@@ -153,6 +153,7 @@ __device__ __forceinline__ int rows_pad_of(int nrows) {
   return nrows <= 8 ? 8 : nrows <= 16 ? 16 : nrows <= 32 ? 32 : nrows <= 64 ? 64 : 128;
 }
 
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
@@ -728,7 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_wait_ld_regs(ra);
           mask16(ra, c, j_lo, j_hi);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
+          for (int j = 0; j < 16; j += 2)
+            mx[(j >> 1) & 3] = tc::max3(mx[(j >> 1) & 3], __uint_as_float(ra[j]), __uint_as_float(ra[j + 1]));
         }
         if (want_max) m_run = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
       }
@@ -753,10 +755,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; j += 2) {
           const float x0 = __uint_as_float(raw[j]), x1 = __uint_as_float(raw[j + 1]);
-          mx[(j >> 1) & 3] = fmaxf(mx[(j >> 1) & 3], fmaxf(x0, x1));
-          const float p0 = ex2(fmaf(x0, sc, neg_m));
-          const float p1 = ex2(fmaf(x1, sc, neg_m));
-          rs[(j >> 1) & 3] += p0 + p1;
+          mx[(j >> 1) & 3] = tc::max3(mx[(j >> 1) & 3], x0, x1);
+          float y0, y1;
+          tc::ffma2(y0, y1, x0, x1, sc, neg_m);
+          const float p0 = ex2(y0), p1 = ex2(y1);
+          if (j & 2)
+            tc::fadd2(rs[2], rs[3], p0, p1);
+          else
+            tc::fadd2(rs[0], rs[1], p0, p1);
           pk[j / 2] = cvt_pair(p0, p1);
         }
         tc::tmem_st8(pcol + 8 * (g0 + c), pk);

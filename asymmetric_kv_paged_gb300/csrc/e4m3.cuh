@@ -39,4 +39,20 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 raw, uint4 &lo, uint
   hi = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
+// 16 E4M3 codes -> 16 fp16 values, also exact (every E4M3 value is an fp16
+// value); one cvt.rn.f16x2.e4m3x2 per pair of codes, low byte to low half.
+// The NaN codes stay NaN here.
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 raw, uint4 &lo, uint4 &hi) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    asm("{\n .reg .b16 l, u;\n mov.b32 {l, u}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n"
+        " cvt.rn.f16x2.e4m3x2 %1, u;\n}\n"
+        : "=r"(h[2 * q]), "=r"(h[2 * q + 1])
+        : "r"(w[q]));
+  lo = make_uint4(h[0], h[1], h[2], h[3]);
+  hi = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
 }  // namespace akp

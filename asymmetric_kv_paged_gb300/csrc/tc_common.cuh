@@ -27,6 +27,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival for the whole warp: every lane's earlier writes are ordered
+// before it by __syncwarp, then lane 0 arrives.  A barrier fed by N warps is
+// initialised with count N: 32 separate arrivals per warp on one barrier are
+// processed one by one and hold its completion back by hundreds of cycles.
+// Lanes publishing shared-memory writes to the async proxy (or TMEM stores to
+// the tensor pipe) issue their fence before calling this.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t *bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // One bounded attempt: the thread sleeps in hardware until the phase with the
 // given parity completes or about `suspend_ns` pass (a hint), instead of
 // polling the barrier in a tight loop.
@@ -109,6 +120,31 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity,
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- paired fp32
+
+// max(a, b, c) in one instruction (three-input max of sm_100-family PTX).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (y0, y1) = (x0, x1) * b + c with one paired fp32 FMA.
+__device__ __forceinline__ void ffma2(float &y0, float &y1, float x0, float x1, float b, float c) {
+  asm("{\n .reg .b64 x, b, c, y;\n mov.b64 x, {%2, %3};\n mov.b64 b, {%4, %4};\n"
+      " mov.b64 c, {%5, %5};\n fma.rn.f32x2 y, x, b, c;\n mov.b64 {%0, %1}, y;\n}\n"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(b), "f"(c));
+}
+
+// (s0, s1) += (x0, x1) with one paired fp32 add.
+__device__ __forceinline__ void fadd2(float &s0, float &s1, float x0, float x1) {
+  asm("{\n .reg .b64 s, x;\n mov.b64 s, {%0, %1};\n mov.b64 x, {%2, %3};\n"
+      " add.f32x2 s, s, x;\n mov.b64 {%0, %1}, s;\n}\n"
+      : "+f"(s0), "+f"(s1)
+      : "f"(x0), "f"(x1));
 }
 
 // ---------------------------------------------------------------- fences
@@ -229,6 +265,35 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[16]) {
                :
                : "memory");
 }
+// Wait for this thread's TMEM loads, naming two 32-register destinations as
+// operands so that no use of them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_wait_ld_regs64(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
+                 "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]),
+                 "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]),
+                 "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]),
+                 "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]),
+                 "+r"(a[30]), "+r"(a[31]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]),
+                 "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]),
+                 "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]),
+                 "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]),
+                 "+r"(b[22]), "+r"(b[23]), "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]),
+                 "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
+               :
+               : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }

@@ -103,7 +103,8 @@ def test_parity_small(case):
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_v_path_bit_exact(P, kv):
     """window 1 with n = L: every row sees only its own key, p = 2^0 = 1 exactly,
-    so the output is that key's V row converted to bf16 without rounding."""
+    so the output is that key's V row converted to bf16 without rounding (the
+    sign of a zero aside)."""
     L = 300
     w = W.make_workload(7, [L], [L], hq=4, hkv=2, page_size=P, window=1, kv_dtype=kv)
     w.v_scale = 1.0
@@ -120,8 +121,12 @@ def test_v_path_bit_exact(P, kv):
         f = torch.from_numpy(vc.copy()).view(torch.float8_e4m3fn).to(torch.bfloat16)
         expect = f.view(torch.int16).numpy().view(np.uint16)
     G = w.hq // w.hkv
+    # -0 may come out as +0: the accumulator adds the zero products of masked keys
+    plus0 = lambda bits: np.where(bits == 0x8000, 0, bits)  # noqa: E731
     for h in range(w.hq):
-        assert np.array_equal(got[:, h], expect[:, h // G]), f"head {h}"
+        bad = np.argwhere(plus0(got[:, h]) != plus0(expect[:, h // G]))
+        assert len(bad) == 0, (f"head {h}: {len(bad)} elements differ, first (token, column, got, "
+                               f"expected): {[(int(t_), int(c), hex(got[t_, h, c]), hex(expect[t_, h // G, c])) for t_, c in bad[:6]]}")
 
 
 @pytest.mark.parametrize("P", [1, 16, 128])
