@@ -14,10 +14,11 @@
 //   warps 4-7   the same for Q tile 1;
 //   warps 8-11  load warps: per key tile, the page lookup of each key, K and V
 //               rows read from the cache with 16-byte loads (one thread per
-//               key), E4M3 widened exactly in registers (K to bf16, the type
-//               of Q; V to fp16, the type of P for FP8 caches), and the rows
-//               stored into the 128-byte-swizzled operand tiles; the Q rows of
-//               each new block;
+//               key), E4M3 widened exactly to fp16 in registers (the MMAs of
+//               an FP8 cache run in fp16), and the rows stored into the
+//               128-byte-swizzled operand tiles; the Q rows of each new block
+//               (for FP8 caches scaled per row by a power of two, see
+//               q_row_shift);
 //   warp  12    TMEM allocation; one thread issues the MMAs of Q tile 0;
 //   warp  13    one thread issues the MMAs of Q tile 1;
 //   warps 14-15 idle (they complete the fourth warpgroup).
@@ -28,8 +29,9 @@
 // Per Q tile t and key tile k: S_t = Q_t.K^T, softmax, O_t += P_t.V.  S_t of
 // tile k+1 is issued only once P_t.V of tile k is done (P_t lives in S_t's
 // columns); the two Q tiles' chains run from separate issuing threads, so one
-// tile's MMAs fill the tensor pipe while the other waits.  Every wait is bounded in time; a broken invariant ends the
-// kernel with bit 1 of the plan's error word set instead of hanging the GPU.
+// tile's MMAs fill the tensor pipe while the other waits.  Every wait is
+// bounded in time; a broken invariant ends the kernel with bit 1 of the plan's
+// error word set instead of hanging the GPU.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 

@@ -162,10 +162,16 @@ attn_status_t attn_plan_replayable(const attn_problem_t *bounds, int device, att
  *   workspace    device scratch of at least workspace_bytes (may be NULL when
  *                the plan reported 0).  Its contents need no initialisation.
  * Slots of the caches that no query can see are never read, so they may hold
- * anything (NaN included).  Queries are used as the bf16 values given, for
- * either cache type: E4M3 elements are widened exactly to bf16 and every
- * product is bf16 x bf16 with fp32 accumulation.  The E4M3 NaN codes (0x7F,
- * 0xFF) in a visible slot are not propagated (they read as +-480).
+ * anything (NaN included).  Queries keep their full bf16 range for either
+ * cache type.  Plans whose row blocks hold at most 128 rows (decode, verify)
+ * widen E4M3 elements exactly to bf16 and form every product as bf16 x bf16
+ * with fp32 accumulation.  Plans with larger blocks (chunked prefill) run
+ * Q.K^T on an FP8 cache in fp16: each query row is multiplied by the power of
+ * two that puts its largest |q| in [2^14, 2^15) (exact; every element down to
+ * 2^-31 of that maximum stays exact in fp16), E4M3 is widened exactly to
+ * fp16, and the scores are divided by the same power of two in fp32; P.V
+ * is fp16 x fp16 with fp32 accumulation.  The E4M3 NaN codes (0x7F, 0xFF) in
+ * a visible slot are not propagated (they read as +-480).
  * Runs of one plan must be ordered on one stream (they share the plan's
  * device error word); different plans are independent.
  * Errors: INVALID_ARG, WORKSPACE, CUDA (launch errors; nothing is waited for).
