@@ -27,9 +27,10 @@
 // tile t at [256 + 128t, 384 + 128t); P (16-bit pairs) overwrites the last 64
 // columns of its S once the softmax has read them.
 // Per Q tile t and key tile k: S_t = Q_t.K^T, softmax, O_t += P_t.V.  S_t of
-// tile k+1 is issued only once P_t.V of tile k is done (P_t lives in S_t's
-// columns); the two Q tiles' chains run from separate issuing threads, so one
-// tile's MMAs fill the tensor pipe while the other waits.  Every wait is
+// tile k+1 is issued right behind P_t.V of tile k (P_t lives in S_t's
+// columns; one thread's MMAs run in issue order); the two Q tiles' chains run
+// from separate issuing threads, so one tile's MMAs fill the tensor pipe while
+// the other waits for its softmax.  Every wait is
 // bounded in time; a broken invariant ends the kernel with bit 1 of the plan's
 // error word set instead of hanging the GPU.
 #include <cuda_bf16.h>
@@ -501,8 +502,10 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArg
         if (first && !tc::mbar_wait_spin(&bars.q_full, cm.si & 1, &abort_flag)) break;
         if (!tc::mbar_wait_spin(&bars.k_full[s], (k >> 1) & 1, &abort_flag)) break;
         if (mine) {
-          // S_t of this tile overwrites P_t of the previous one
-          if (ct > 0 && !tc::mbar_wait_spin(&bars.pv_done[t], (ct - 1) & 1, &abort_flag)) break;
+          // S_t of this tile overwrites P_t of the previous one, which P_t.V
+          // reads: that MMA was issued before these by this same thread, and
+          // the tensor pipe runs one thread's MMAs in issue order, so there
+          // is nothing to wait for.
           // The two Q tiles take turns: S1 of a tile is issued once S0 of it is
           // done, S0 once S1 of the previous tile is.  Their softmaxes then run
           // half a tile apart, each while the tensor pipe works for the other,
@@ -657,32 +660,75 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArg
       };
       max32(s0);
       max32(s1);
-      max32(s2);
-      max32(s3);
-      const float m_tile = fmaxf(mx[0], mx[1]) * sc;
-      // O is rescaled only when the maximum grows by more than the threshold;
-      // until then P may exceed 1 (up to 2^8)
-      const bool need = m_run != -INFINITY && m_tile > m_run + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        if (!wait(&bars.pv_done[t], (c - 1) & 1)) break;
-        tc::tc_fence_after();
-        const float alpha = need ? ex2(m_run - m_tile) : 1.f;
-#pragma unroll 1
-        for (int q = 0; q < kDv / 16; ++q) {
-          uint32_t o[16];
-          tc::tmem_ld16(o_addr + q * 16, o);
-          tc::tmem_wait_ld_regs(o);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tc::tmem_st16(o_addr + q * 16, o);
-        }
-        tc::tmem_wait_st();
-        l_run *= alpha;
-      }
-      if (need || m_run == -INFINITY) m_run = m_tile;
-      // P = 2^(s * sc - m_run), 16-bit pairs; masked columns are -inf already
-      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+      const float m_lo = fmaxf(mx[0], mx[1]) * sc;
+      // Keys 64-127 are exponentiated against m_base, the running maximum (on
+      // a row's first tile the maximum of keys 0-63), while their own maximum
+      // is taken, so their exponents need not wait for a maximum pass.  Only
+      // when the tile's maximum exceeds m_base by more than the threshold
+      // (rare once the maximum has settled) is O rescaled and the pass redone
+      // from S, which is still in TMEM.  Until then P may exceed 1 (up to 2^8).
+      float m_base = m_run != -INFINITY ? m_run : m_lo;
       float rs[2] = {0.f, 0.f};
+      float mh[2] = {-INFINITY, -INFINITY};
+      uint32_t pk2[16], pk3[16];
+      auto exp_pack = [&](const uint32_t (&raw)[32], uint32_t (&pk)[16], float nm, bool track) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float x0 = __uint_as_float(raw[j]), x1 = __uint_as_float(raw[j + 1]);
+          if (track) mh[(j >> 1) & 1] = tc::max3(mh[(j >> 1) & 1], x0, x1);
+          float y0, y1;
+          tc::ffma2(y0, y1, x0, x1, sc, nm);
+          const float p0 = ex2(y0), p1 = ex2(y1);
+          tc::fadd2(rs[0], rs[1], p0, p1);
+          pk[j >> 1] = FP8 ? f16_pair(p0, p1) : bf16_pair(p0, p1);
+        }
+      };
+      exp_pack(s2, pk2, m_base == -INFINITY ? 0.f : -m_base, true);
+      exp_pack(s3, pk3, m_base == -INFINITY ? 0.f : -m_base, true);
+      const float m_tile = fmaxf(m_lo, fmaxf(mh[0], mh[1]) * sc);
+      const bool need = m_tile > m_base + kRescaleThreshold;   // never for m_tile = -inf
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? m_tile : m_base;
+        // O holds earlier tiles' sums only where the running maximum is finite
+        const bool rescale = need && m_run != -INFINITY;
+        if (__any_sync(0xffffffffu, rescale)) {
+          if (!wait(&bars.pv_done[t], (c - 1) & 1)) break;
+          tc::tc_fence_after();
+          const float alpha = rescale ? ex2(m_run - m_new) : 1.f;
+#pragma unroll 1
+          for (int q = 0; q < kDv / 16; ++q) {
+            uint32_t o[16];
+            tc::tmem_ld16(o_addr + q * 16, o);
+            tc::tmem_wait_ld_regs(o);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tc::tmem_st16(o_addr + q * 16, o);
+          }
+          tc::tmem_wait_st();
+          l_run *= alpha;
+        }
+        m_base = m_new;
+        tc::tmem_ld32(s_addr + 64, s2);
+        tc::tmem_ld32(s_addr + 96, s3);
+        tc::tmem_wait_ld_regs64(s2, s3);
+        if (!full) {
+          mask32(s2, 64);
+          mask32(s3, 96);
+        }
+        rs[0] = rs[1] = 0.f;
+        exp_pack(s2, pk2, m_base == -INFINITY ? 0.f : -m_base, false);
+        exp_pack(s3, pk3, m_base == -INFINITY ? 0.f : -m_base, false);
+      }
+      m_run = m_base;
+      // P_t: key j's 16-bit value in the low (even j) or high half of TMEM
+      // column 64 + j/2 of S_t; keys 64-127 first, so that half of P.V starts
+      // while keys 0-63 are exponentiated
+      tc::tmem_st16(s_addr + kPN / 2 + 32, pk2);
+      tc::tmem_st16(s_addr + kPN / 2 + 48, pk3);
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      tc::mbar_arrive_warp(&bars.p_hi[t]);
+      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
       auto exp32 = [&](const uint32_t (&raw)[32], int c0) {
 #pragma unroll
         for (int h = 0; h < 32; h += 16) {
@@ -698,11 +744,6 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArg
           tc::tmem_st8(s_addr + kPN / 2 + (c0 + h) / 2, pk);
         }
       };
-      exp32(s2, 64);                       // keys 64-127 first: half of P.V starts early
-      exp32(s3, 96);
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-      tc::mbar_arrive_warp(&bars.p_hi[t]);
       exp32(s0, 0);
       exp32(s1, 32);
       tc::tmem_wait_st();                  // P is in TMEM before p_full is signalled
