@@ -45,7 +45,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// K (d = 192) or V (d = 128) cache as a 3D tensor [slots][Hkv][d]; boxes of
+// K (d = 192 or 128) or V (d = 128) cache as a 3D tensor [slots][Hkv][d]; boxes of
 // `rows` consecutive slots of one head: 64 bf16 columns with 128-byte swizzle
 // (the tensor-core operand layout), or whole raw E4M3 rows without swizzle.
 bool make_cache_map(CUtensorMap *map, const void *base, bool fp8, int d, int hkv, int64_t slots,
@@ -256,7 +256,7 @@ static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const
       return ATTN_ERR_INVALID_ARG;
     const int64_t slots = (int64_t)pr.num_pages * pr.page_size;
     const int rows = pr.page_size >= akp::kKeyTile ? akp::kKeyTile : pr.page_size;
-    if (!make_cache_map(&maps.k, k_cache, fp8, akp::kDqk, pr.num_kv_heads, slots, rows) ||
+    if (!make_cache_map(&maps.k, k_cache, fp8, pr.head_dim_qk, pr.num_kv_heads, slots, rows) ||
         !make_cache_map(&maps.v, v_cache, fp8, akp::kDv, pr.num_kv_heads, slots, rows))
       return ATTN_ERR_CUDA;
   }

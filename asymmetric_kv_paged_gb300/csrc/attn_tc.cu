@@ -45,10 +45,16 @@ namespace {
 constexpr int kN = kKeyTile;                 // keys per tile (64)
 constexpr int kThreads = 11 * 32;
 constexpr int kBlk = kN * 128;               // one 64-column block of a 64-row tile: 8 KB
-constexpr int kOpK = 3 * kBlk;               // K operand tile: 24 KB
-constexpr int kOpBytes = kOpK + 2 * kBlk;    // + V operand tile: 40 KB
-constexpr int kRawK = kN * kDqk;             // raw E4M3 K rows: 12 KB
-constexpr int kRawBytes = kRawK + kN * kDv;  // + raw V rows: 20 KB
+// Tile sizes for query/key head dim DQK (192, or 128 for layers with a
+// symmetric head-dim pair; the value head dim is 128 either way).
+template <int DQK>
+struct Dims {
+  static_assert(DQK % 64 == 0, "the K tile is made of 64-column blocks");
+  static constexpr int kOpK = (DQK / 64) * kBlk;       // K operand tile: 24 KB at 192
+  static constexpr int kOpBytes = kOpK + 2 * kBlk;      // + V operand tile: 40 KB at 192
+  static constexpr int kRawK = kN * DQK;                // raw E4M3 K rows: 12 KB at 192
+  static constexpr int kRawBytes = kRawK + kN * kDv;    // + raw V rows: 20 KB at 192
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 128;             // O: 128 fp32 columns
 constexpr uint32_t kTmemP = 256;             // P double buffer: 2 x 32 columns (bf16 pairs)
@@ -65,10 +71,12 @@ struct SlotBars {
 // Shared-memory layout for MR MMA rows (64 or 128): Q as three 64-column
 // blocks of MR rows (two buffers where they fit), the K/V operand ring, the
 // FP8 staging ring and the epilogue's copy-combine buffer.  P lives in TMEM.
-template <bool FP8, int MR, bool TMA>
+template <bool FP8, int MR, bool TMA, int DQK>
 struct Layout {
+  static constexpr int kOpBytes = Dims<DQK>::kOpBytes;
+  static constexpr int kRawBytes = Dims<DQK>::kRawBytes;
   static constexpr int kQBlock = MR * 128;    // one 64-column block of Q
-  static constexpr int kQBytes = 3 * kQBlock;
+  static constexpr int kQBytes = (DQK / 64) * kQBlock;
   // Q is double-buffered where it fits (BF16, M = 64): the next segment's
   // rows are staged while the current one runs.
   static constexpr int kQBufs = (!FP8 && MR == 64) ? 2 : 1;
@@ -180,14 +188,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-template <bool FP8, bool TMA, int MR>
+template <bool FP8, bool TMA, int MR, int DQK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const RunArgs args, const __grid_constant__ TmaMaps maps) {
   // A plain local copy of the arguments: the role lambdas capture by reference,
   // and a reference into kernel-parameter space would turn every field read
   // inside them into a memory load that the K/V stream keeps evicting.
   const RunArgs a = args;
-  using Lay = Layout<FP8, MR, TMA>;
+  using Lay = Layout<FP8, MR, TMA, DQK>;
+  // this instantiation's query/key head dim and tile sizes
+  constexpr int kDqk = DQK;
+  constexpr int kOpK = Dims<DQK>::kOpK;
+  constexpr int kOpBytes = Dims<DQK>::kOpBytes;
+  constexpr int kRawK = Dims<DQK>::kRawK;
+  constexpr int kRawBytes = Dims<DQK>::kRawBytes;
   constexpr int kRows = MR;                 // MMA rows (M)
   constexpr int kQBlock = Lay::kQBlock;
   constexpr int NS = Lay::kOpStages;
@@ -344,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(dst + kRawK + i * box * kDv, &maps.v, 0, bd.g, slot[i], full);
           } else {
 #pragma unroll
-            for (int c = 0; c < 3; ++c)
+            for (int c = 0; c < kDqk / 64; ++c)
               tma_load_3d(dst + c * kBlk + i * box * 128, &maps.k, 64 * c, bd.g, slot[i],
                           full);
 #pragma unroll
@@ -373,8 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       uint8_t *qs = smem + qb * Lay::kQBytes;
       const int rows_pad = rows_pad_of(bd.nrows);
-      constexpr int kIters = kRows * 24 / 128;
-      constexpr int kBatch = kRows == 128 ? 8 : 12;
+      constexpr int kQch = kDqk / 8;       // 16-byte chunks per Q row
+      constexpr int kIters = kRows * kQch / 128;
+      constexpr int kBatch = kRows == 64 && kIters % 12 == 0 ? 12 : 8;
       static_assert(kIters % kBatch == 0, "Q staging batches");
 #pragma unroll 1
       for (int i0 = 0; i0 < kIters; i0 += kBatch) {
@@ -382,9 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int idx = ct + (i0 + u) * 128;
-          const int p = idx / 24;          // MMA row position
+          const int p = idx / kQch;        // MMA row position
           const int r = p % rows_pad;      // block row it holds
-          const int ch = idx % 24;
+          const int ch = idx % kQch;
           v[u] = make_uint4(0u, 0u, 0u, 0u);
           if (r < bd.nrows) {
             const int flat = bd.row0 + r;
@@ -397,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int idx = ct + (i0 + u) * 128;
-          const int p = idx / 24;
-          const int ch = idx % 24;
+          const int p = idx / kQch;
+          const int ch = idx % kQch;
           *reinterpret_cast<uint4 *>(qs + (ch >> 3) * kQBlock + tc::sw128_offset(p, ch & 7)) = v[u];
         }
       }
@@ -1020,31 +1035,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool FP8, bool TMA, int MR>
+template <bool FP8, bool TMA, int MR, int DQK>
 cudaError_t launch_one(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
-  attn_tc_kernel<FP8, TMA, MR><<<hp.num_ctas, kThreads, Layout<FP8, MR, TMA>::kSmem, st>>>(a, m);
+  attn_tc_kernel<FP8, TMA, MR, DQK>
+      <<<hp.num_ctas, kThreads, Layout<FP8, MR, TMA, DQK>::kSmem, st>>>(a, m);
   return cudaGetLastError();
 }
 
-template <bool FP8, bool TMA, int MR>
+template <bool FP8, bool TMA, int MR, int DQK>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(attn_tc_kernel<FP8, TMA, MR>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<FP8, MR, TMA>::kSmem);
+  return cudaFuncSetAttribute(attn_tc_kernel<FP8, TMA, MR, DQK>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Layout<FP8, MR, TMA, DQK>::kSmem);
 }
 
-template <int MR>
+template <int MR, int DQK>
 cudaError_t launch_rows(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
   const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
   if (hp.use_tma)
-    return fp8 ? launch_one<true, true, MR>(hp, a, m, st) : launch_one<false, true, MR>(hp, a, m, st);
-  return fp8 ? launch_one<true, false, MR>(hp, a, m, st) : launch_one<false, false, MR>(hp, a, m, st);
+    return fp8 ? launch_one<true, true, MR, DQK>(hp, a, m, st)
+               : launch_one<false, true, MR, DQK>(hp, a, m, st);
+  return fp8 ? launch_one<true, false, MR, DQK>(hp, a, m, st)
+             : launch_one<false, false, MR, DQK>(hp, a, m, st);
 }
 
-template <int MR>
+template <int MR, int DQK>
 cudaError_t prepare_rows(const HostPlan &hp) {
   const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
-  if (hp.use_tma) return fp8 ? prepare_one<true, true, MR>() : prepare_one<false, true, MR>();
-  return fp8 ? prepare_one<true, false, MR>() : prepare_one<false, false, MR>();
+  if (hp.use_tma) return fp8 ? prepare_one<true, true, MR, DQK>() : prepare_one<false, true, MR, DQK>();
+  return fp8 ? prepare_one<true, false, MR, DQK>() : prepare_one<false, false, MR, DQK>();
 }
 
 }  // namespace
@@ -1057,12 +1076,17 @@ bool tc_tma_page_size(int32_t page_size, int32_t num_pages) {
 cudaError_t launch_attn_tc(const HostPlan &hp, const RunArgs &a, const TmaMaps &m,
                            cudaStream_t stream) {
   if (hp.num_ctas == 0) return cudaSuccess;
-  return hp.block_rows == 64 ? launch_rows<64>(hp, a, m, stream)
-                             : launch_rows<128>(hp, a, m, stream);
+  if (hp.prob.head_dim_qk == kDqkSym)
+    return hp.block_rows == 64 ? launch_rows<64, 128>(hp, a, m, stream)
+                               : launch_rows<128, 128>(hp, a, m, stream);
+  return hp.block_rows == 64 ? launch_rows<64, kDqk>(hp, a, m, stream)
+                             : launch_rows<128, kDqk>(hp, a, m, stream);
 }
 
 cudaError_t prepare_attn_tc(const HostPlan &hp) {
-  return hp.block_rows == 64 ? prepare_rows<64>(hp) : prepare_rows<128>(hp);
+  if (hp.prob.head_dim_qk == kDqkSym)
+    return hp.block_rows == 64 ? prepare_rows<64, 128>(hp) : prepare_rows<128, 128>(hp);
+  return hp.block_rows == 64 ? prepare_rows<64, kDqk>(hp) : prepare_rows<128, kDqk>(hp);
 }
 
 }  // namespace akp

@@ -25,17 +25,16 @@
 namespace akp {
 namespace {
 
-constexpr int kKChunks = kDqk / 8;   // 24
-constexpr int kVChunks = kDv / 8;    // 16
-constexpr int kChunks = kKChunks + kVChunks;
+constexpr int kVChunks = kDv / 8;    // 16-byte bf16 chunks of a V row: 16
 
 struct AppendArgs {
   const uint16_t *k_new, *v_new;
   void *k_cache, *v_cache;
   const int32_t *page_table, *seq_lens, *qo_indptr;
   int32_t *err;
-  int64_t units;            // total_q * hkv * kChunks
+  int64_t units;            // total_q * hkv * (k_chunks + 16)
   int32_t batch, hkv, page_size, pt_stride, num_pages;
+  int32_t dqk, k_chunks;    // query/key head dim, 16-byte chunks of a K row (dqk / 8)
   float k_scale, v_scale;
 };
 
@@ -50,8 +49,9 @@ template <bool FP8>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < a.units;
        u += (int64_t)gridDim.x * blockDim.x) {
-    const int chunk = (int)(u % kChunks);
-    const int64_t pair = u / kChunks;
+    const int chunks = a.k_chunks + kVChunks;
+    const int chunk = (int)(u % chunks);
+    const int64_t pair = u / chunks;
     const int g = (int)(pair % a.hkv);
     const int tok = (int)(pair / a.hkv);
     // request of this token: last b with qo_indptr[b] <= tok
@@ -73,9 +73,9 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
       continue;
     }
     const int64_t slot = (int64_t)page * a.page_size + i % a.page_size;
-    const bool is_k = chunk < kKChunks;
-    const int c = is_k ? chunk : chunk - kKChunks;
-    const int D = is_k ? kDqk : kDv;
+    const bool is_k = chunk < a.k_chunks;
+    const int c = is_k ? chunk : chunk - a.k_chunks;
+    const int D = is_k ? a.dqk : kDv;
     const uint4 src = __ldg(reinterpret_cast<const uint4 *>((is_k ? a.k_new : a.v_new) +
                                                             ((int64_t)tok * a.hkv + g) * D) + c);
     const int64_t row = (slot * a.hkv + g) * D;
@@ -131,7 +131,9 @@ extern "C" attn_status_t attn_append_kv(attn_plan_t plan, const void *k_new, con
   a.seq_lens = seq_lens;
   a.qo_indptr = qo_indptr;
   a.err = plan->dev.err;
-  a.units = total_q * pr.num_kv_heads * akp::kChunks;
+  a.dqk = pr.head_dim_qk;
+  a.k_chunks = pr.head_dim_qk / 8;
+  a.units = total_q * pr.num_kv_heads * (a.k_chunks + akp::kVChunks);
   a.batch = pr.batch;
   a.hkv = pr.num_kv_heads;
   a.page_size = pr.page_size;

@@ -10,6 +10,7 @@
 namespace akp {
 
 constexpr int kDqk = 192;       // query/key head dim
+constexpr int kDqkSym = 128;    // query/key head dim of the symmetric pair 128/128
 constexpr int kDv = 128;        // value head dim
 constexpr int kKeyTile = 64;    // keys per pipeline tile (decode / verify kernel)
 constexpr int kPrefillKeyTile = 128;   // keys per tile of the prefill kernel

@@ -25,7 +25,12 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
       p->num_pages <= 0 || p->page_table_stride <= 0)
     return ATTN_ERR_INVALID_ARG;
   if (p->batch > 0 && (!p->qo_indptr_host || !p->seq_lens_host)) return ATTN_ERR_INVALID_ARG;
-  if (p->head_dim_qk != kDqk || p->head_dim_v != kDv) return ATTN_ERR_UNSUPPORTED;
+  // Head-dim pairs: 192/128 (MiMo's layers), and 128/128 for layers whose
+  // own pair is symmetric (sglang PR #32818, "Three changes", item 1: a model
+  // is asymmetric when head_dim != v_head_dim or swa_head_dim !=
+  // swa_v_head_dim, so its SWA layers may carry a pair of their own).
+  if ((p->head_dim_qk != kDqk && p->head_dim_qk != kDqkSym) || p->head_dim_v != kDv)
+    return ATTN_ERR_UNSUPPORTED;
   if (p->num_q_heads % p->num_kv_heads != 0) return ATTN_ERR_UNSUPPORTED;
   if (p->kv_dtype != ATTN_KV_BF16 && p->kv_dtype != ATTN_KV_FP8_E4M3) return ATTN_ERR_UNSUPPORTED;
 
@@ -48,7 +53,7 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
     if ((L + p->page_size - 1) / p->page_size > p->page_table_stride) return ATTN_ERR_INVALID_ARG;
   }
   // Flat row and tile counts must stay inside int32 device arithmetic.
-  if ((int64_t)hp.qo_indptr[p->batch] * p->num_q_heads > INT32_MAX / kDqk)
+  if ((int64_t)hp.qo_indptr[p->batch] * p->num_q_heads > INT32_MAX / p->head_dim_qk)
     return ATTN_ERR_UNSUPPORTED;
 
   hp.threads = 352;
@@ -58,7 +63,8 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   // M = 64 halves the Q and P tiles, so one more K/V stage fits (and Q can be
   // double-buffered); for blocks of up to 64 rows that beats M = 128's second
   // row copy, measured on 8- and 64-row blocks.
-  hp.block_rows = max_rows <= 64 ? 64 : max_rows <= 128 ? 128 : 256;
+  // (the prefill kernel is built for the 192/128 pair only)
+  hp.block_rows = max_rows <= 64 ? 64 : max_rows <= 128 || p->head_dim_qk != kDqk ? 128 : 256;
   hp.prefill = hp.block_rows == 256;
   hp.key_tile = hp.prefill ? kPrefillKeyTile : kKeyTile;
   const int32_t rows_per_block = hp.block_rows;

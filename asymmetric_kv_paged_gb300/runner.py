@@ -47,7 +47,7 @@ class DeviceWorkload:
             num_pages=w.num_pages, page_table_stride=w.page_table.shape[1],
             kv_dtype=B.ATTN_KV_BF16 if w.kv_dtype == "bf16" else B.ATTN_KV_FP8_E4M3,
             window=w.window, has_sinks=w.sinks is not None, qo_indptr=w.qo_indptr,
-            seq_lens=w.seq_lens)
+            seq_lens=w.seq_lens, head_dim_qk=w.dqk)
 
     def make_plan(self):
         prob, keep = self.problem()

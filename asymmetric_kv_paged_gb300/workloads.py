@@ -92,14 +92,15 @@ class Workload:
     qo_indptr: np.ndarray            # int32 [B+1]
     seq_lens: np.ndarray             # int32 [B]
     page_table: np.ndarray           # int32 [B, stride]
-    q: np.ndarray                    # uint16 (bf16 bits) [total_q, Hq, 192]
-    k_cache: np.ndarray              # uint16 | uint8 [num_pages, P, Hkv, 192]
+    q: np.ndarray                    # uint16 (bf16 bits) [total_q, Hq, Dqk] (Dqk 192 or 128)
+    k_cache: np.ndarray              # uint16 | uint8 [num_pages, P, Hkv, Dqk]
     v_cache: np.ndarray              # uint16 | uint8 [num_pages, P, Hkv, 128]
     sinks: np.ndarray | None         # float32 [Hq] or None
     softmax_scale: float
     k_scale: float = 1.0
     v_scale: float = 1.0
     meta: dict = field(default_factory=dict)
+    dqk: int = DQK                   # query/key head dim (the value head dim is 128)
 
     @property
     def batch(self) -> int:
@@ -131,8 +132,9 @@ def make_workload(seed: int, seq_lens, n_per_req, hq: int, hkv: int, page_size: 
                   kv_dtype: str = "bf16", k_std: float = 1.0, v_std: float = 1.0,
                   q_std: float = 1.0, softmax_scale: float | None = None,
                   name: str = "custom", rng: np.random.Generator | None = None,
-                  pages_in_order: bool = False) -> Workload:
-    """Build one workload.  `seq_lens` and `n_per_req` are per request (n <= L)."""
+                  pages_in_order: bool = False, dqk: int = DQK) -> Workload:
+    """Build one workload.  `seq_lens` and `n_per_req` are per request (n <= L);
+    `dqk` is the query/key head dim (the value head dim is 128)."""
     rng = rng if rng is not None else np.random.default_rng(seed)
     seq = np.asarray(seq_lens, dtype=np.int64)
     n = np.asarray(n_per_req, dtype=np.int64)
@@ -156,7 +158,7 @@ def make_workload(seed: int, seq_lens, n_per_req, hq: int, hkv: int, page_size: 
     qo_indptr = np.zeros(B + 1, dtype=np.int32)
     qo_indptr[1:] = np.cumsum(n)
     total_q = int(qo_indptr[-1])
-    q = bf16_bits(rng.standard_normal((total_q, hq, DQK), dtype=np.float32) * np.float32(q_std))
+    q = bf16_bits(rng.standard_normal((total_q, hq, dqk), dtype=np.float32) * np.float32(q_std))
 
     # slots that some query can see
     slot_lists = []
@@ -171,16 +173,16 @@ def make_workload(seed: int, seq_lens, n_per_req, hq: int, hkv: int, page_size: 
 
     nslot = num_pages * page_size
     kv_seed = int(rng.integers(0, 2**63 - 1))
-    k_vals = _draw_rows(kv_seed, 0, slots.size, hkv * DQK, k_std)
+    k_vals = _draw_rows(kv_seed, 0, slots.size, hkv * dqk, k_std)
     v_vals = _draw_rows(kv_seed, 1, slots.size, hkv * DV, v_std)
     if kv_dtype == "bf16":
-        k_cache = np.full((nslot, hkv * DQK), BF16_NAN, dtype=np.uint16)
+        k_cache = np.full((nslot, hkv * dqk), BF16_NAN, dtype=np.uint16)
         v_cache = np.full((nslot, hkv * DV), BF16_NAN, dtype=np.uint16)
         k_cache[slots] = bf16_bits(k_vals)
         v_cache[slots] = bf16_bits(v_vals)
         k_scale = v_scale = 1.0
     elif kv_dtype == "fp8":
-        k_cache = np.full((nslot, hkv * DQK), E4M3_NAN, dtype=np.uint8)
+        k_cache = np.full((nslot, hkv * dqk), E4M3_NAN, dtype=np.uint8)
         v_cache = np.full((nslot, hkv * DV), E4M3_NAN, dtype=np.uint8)
         k_amax = float(np.abs(k_vals).max()) if k_vals.size else 1.0
         v_amax = float(np.abs(v_vals).max()) if v_vals.size else 1.0
@@ -194,19 +196,22 @@ def make_workload(seed: int, seq_lens, n_per_req, hq: int, hkv: int, page_size: 
 
     sink_arr = rng.standard_normal(hq, dtype=np.float32) if sinks else None
     if softmax_scale is None:
-        softmax_scale = 1.0 / math.sqrt(DQK)
+        softmax_scale = 1.0 / math.sqrt(dqk)
     return Workload(name=name, hq=hq, hkv=hkv, page_size=page_size, num_pages=num_pages,
                     window=window, kv_dtype=kv_dtype, qo_indptr=qo_indptr,
                     seq_lens=seq.astype(np.int32), page_table=page_table, q=q,
-                    k_cache=k_cache.reshape(num_pages, page_size, hkv, DQK),
+                    k_cache=k_cache.reshape(num_pages, page_size, hkv, dqk),
                     v_cache=v_cache.reshape(num_pages, page_size, hkv, DV),
                     sinks=sink_arr, softmax_scale=float(softmax_scale),
-                    k_scale=k_scale, v_scale=v_scale)
+                    k_scale=k_scale, v_scale=v_scale, dqk=dqk)
 
 
 # ---------------------------------------------------------------------------
 # The named workloads.  C3 comes in two page sizes (a: 128, b: 1).
 
+# Further measured shapes (not among the configs above): an SWA layer with a
+# symmetric head-dim pair of its own.
+EXTRA_NAMES = ("c4s_swa_sinks_d128",)
 CONFIG_NAMES = ("c1_tiny_decode", "c2_batched_decode", "c3a_verify_p128", "c3b_verify_p1",
                 "c4_swa_sinks", "c5_chunked_prefill")
 
@@ -252,15 +257,17 @@ def verify(page_size: int) -> Workload:
                          num_pages=POOL_SLOTS // page_size, name=name, rng=rng)
 
 
-def swa_sinks() -> Workload:
+def swa_sinks(dqk: int = DQK) -> Workload:
     """64 requests (32 decode + 32 eight-token verify rows, seeded shuffle), L = 8192,
-    window 128, per-head sinks N(0,1), 16/2 heads, page 128."""
+    window 128, per-head sinks N(0,1), 16/2 heads, page 128.  With dqk = 128: the
+    same batch on a sliding-window layer whose own head-dim pair is 128/128."""
     rng = np.random.default_rng(1004)
     seq = np.full(64, 8192, np.int64)
     n = np.array([1] * 32 + [8] * 32, np.int64)
     rng.shuffle(n)
+    name = "c4_swa_sinks" if dqk == DQK else f"c4s_swa_sinks_d{dqk}"
     return make_workload(0, seq, n, hq=16, hkv=2, page_size=128, num_pages=POOL_SLOTS // 128,
-                         window=128, sinks=True, name="c4_swa_sinks", rng=rng)
+                         window=128, sinks=True, name=name, rng=rng, dqk=dqk)
 
 
 def chunked_prefill() -> Workload:
@@ -280,5 +287,6 @@ def named(name: str) -> Workload:
         "c3a_verify_p128": lambda: verify(128),
         "c3b_verify_p1": lambda: verify(1),
         "c4_swa_sinks": swa_sinks,
+        "c4s_swa_sinks_d128": lambda: swa_sinks(128),
         "c5_chunked_prefill": chunked_prefill,
     }[name]()

@@ -54,8 +54,8 @@ def algorithmic_bytes(w) -> int:
         if hi > lo:
             keys += hi - lo
             pages += (hi - 1) // w.page_size - lo // w.page_size + 1
-    total = keys * w.hkv * (DQK + DV) * es
-    total += w.total_q * w.hq * (DQK + DV) * 2
+    total = keys * w.hkv * (w.dqk + DV) * es
+    total += w.total_q * w.hq * (w.dqk + DV) * 2
     total += pages * 4
     if w.sinks is not None:
         total += w.hq * 4
@@ -63,7 +63,7 @@ def algorithmic_bytes(w) -> int:
 
 
 def algorithmic_flops(w) -> int:
-    """2 * (192 + 128) FLOPs per visible (query row, key) pair."""
+    """2 * (Dqk + 128) FLOPs per visible (query row, key) pair (Dqk = 192)."""
     pairs = 0
     for b in range(w.batch):
         L = int(w.seq_lens[b])
@@ -71,7 +71,7 @@ def algorithmic_flops(w) -> int:
         i = L - n + np.arange(n, dtype=np.int64)
         lo = np.maximum(0, i - w.window + 1) if w.window > 0 else np.zeros_like(i)
         pairs += int((i + 1 - lo).sum())
-    return 2 * (DQK + DV) * pairs * w.hq
+    return 2 * (w.dqk + DV) * pairs * w.hq
 
 
 def peaks():
@@ -317,7 +317,7 @@ def e2e_measure(w, steps: int, warmup: int, world: int):
     L0 = w.seq_lens.astype(np.int64)
     rng = np.random.default_rng(7)
     h_q = torch.from_numpy(w.q).view(torch.bfloat16).pin_memory()
-    h_kn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, DQK), dtype=np.float32)).to(
+    h_kn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, w.dqk), dtype=np.float32)).to(
         torch.bfloat16).pin_memory()
     h_vn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, DV), dtype=np.float32)).to(
         torch.bfloat16).pin_memory()
@@ -416,8 +416,8 @@ def cpu_baseline(w, budget_s: float = 12.0):
         oracle.attn_paged(pb, rows=rows)
         t_total += time.time() - t
         lo, hi = w.visible_range(b)
-        done_bytes += (hi - lo) * w.hkv * (DQK + DV) * (2 if w.kv_dtype == "bf16" else 1)
-        done_bytes += len(toks) * w.hq * (DQK + DV) * 2
+        done_bytes += (hi - lo) * w.hkv * (w.dqk + DV) * (2 if w.kv_dtype == "bf16" else 1)
+        done_bytes += len(toks) * w.hq * (w.dqk + DV) * 2
         done_req += 1
         if t_total >= budget_s:
             break
@@ -438,12 +438,12 @@ def measure_append(name: str, pk: dict, steps: int, warmup: int):
     dw = DeviceWorkload(w, device=torch.cuda.current_device(), with_lse=False)
     rng = np.random.default_rng(99)
     dev = torch.device("cuda", torch.cuda.current_device())
-    kn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, DQK), dtype=np.float32)).to(
+    kn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, w.dqk), dtype=np.float32)).to(
         dev).to(torch.bfloat16)
     vn = torch.from_numpy(rng.standard_normal((w.total_q, w.hkv, DV), dtype=np.float32)).to(
         dev).to(torch.bfloat16)
     es = 2 if w.kv_dtype == "bf16" else 1
-    nbytes = (w.total_q * w.hkv * (DQK + DV) * (2 + es) + w.total_q * 4 * 3
+    nbytes = (w.total_q * w.hkv * (w.dqk + DV) * (2 + es) + w.total_q * 4 * 3
               + (w.batch + 1) * 4 + w.batch * 4)
     ks, vs = (w.k_scale, w.v_scale) if w.kv_dtype == "fp8" else (1.0, 1.0)
     stream = torch.cuda.current_stream()
@@ -607,7 +607,7 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_extra:
         extra = []
-        for name in workloads.CONFIG_NAMES:
+        for name in workloads.CONFIG_NAMES + workloads.EXTRA_NAMES:
             if name == args.workload:
                 continue
             extra.append(measure_extra(name, pk, max(20, args.steps // 4), args.warmup, 1))
@@ -633,7 +633,7 @@ def workload_config(w, nbytes: int, world: int) -> dict:
     """The `config` object of the JSON line; both arms report the same one."""
     return {"workload": w.name, "batch": w.batch,
             "q_tokens_per_request": int(w.qo_indptr[1] - w.qo_indptr[0]) if w.batch else 0,
-            "num_q_heads": w.hq, "num_kv_heads": w.hkv, "head_dim_qk": DQK, "head_dim_v": DV,
+            "num_q_heads": w.hq, "num_kv_heads": w.hkv, "head_dim_qk": w.dqk, "head_dim_v": DV,
             "page_size": w.page_size, "pool_slots": w.num_pages * w.page_size,
             "kv_tokens": int(w.seq_lens.sum()), "kv_dtype": w.kv_dtype,
             "algorithmic_bytes_per_step": nbytes,
@@ -656,8 +656,8 @@ def run_reference(args):
         (np.arange(w.qo_indptr[b], w.qo_indptr[b + 1])[:, None] * w.hq
          + np.arange(w.hq)[None, :]).reshape(-1) for b in reqs])
     es = 2 if w.kv_dtype == "bf16" else 1
-    nbytes = sum((w.visible_range(b)[1] - w.visible_range(b)[0]) * w.hkv * (DQK + DV) * es
-                 + int(w.qo_indptr[b + 1] - w.qo_indptr[b]) * w.hq * (DQK + DV) * 2 for b in reqs)
+    nbytes = sum((w.visible_range(b)[1] - w.visible_range(b)[0]) * w.hkv * (w.dqk + DV) * es
+                 + int(w.qo_indptr[b + 1] - w.qo_indptr[b]) * w.hq * (w.dqk + DV) * 2 for b in reqs)
     for _ in range(args.warmup):
         oracle.attn_paged(pb, rows=rows)
     t = time.time()

@@ -53,7 +53,7 @@ typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = -1,  /* a NULL pointer, inconsistent sizes, or a run
                                    argument that does not match the plan */
-    ATTN_ERR_UNSUPPORTED = -2,  /* head dims other than 192/128, Hq % Hkv != 0 */
+    ATTN_ERR_UNSUPPORTED = -2,  /* head dims other than 192/128 or 128/128, Hq % Hkv != 0 */
     ATTN_ERR_WORKSPACE = -3,    /* workspace smaller than attn_plan reported */
     ATTN_ERR_CUDA = -4          /* a CUDA runtime error (allocation in attn_plan,
                                    or a launch error in attn_run_paged) */
@@ -72,7 +72,13 @@ typedef struct attn_plan_s *attn_plan_t;
  * arrays afterwards).
  *   batch               B >= 0 requests.
  *   num_q_heads         Hq; num_kv_heads Hkv; Hq % Hkv == 0.
- *   head_dim_qk         must be 192; head_dim_v must be 128.
+ *   head_dim_qk         192 (the asymmetric pair 192/128), or 128 for a layer
+ *                       whose own pair is symmetric (128/128): a model is
+ *                       asymmetric when head_dim != v_head_dim or
+ *                       swa_head_dim != swa_v_head_dim (sglang PR #32818,
+ *                       "Three changes", item 1), so its sliding-window layers
+ *                       may carry a pair of their own.  head_dim_v must be 128.
+ *                       128/128 plans never use the 256-row prefill kernel.
  *   page_size           P >= 1 tokens per page.
  *   num_pages           pages in each of the K and V pools.
  *   page_table_stride   int32 entries per request row of the page table; must
@@ -131,8 +137,9 @@ attn_status_t attn_plan_replayable(const attn_problem_t *bounds, int device, att
 
 /*
  * Run the planned attention on `stream`.
- *   q            bf16 [total_q, Hq, 192], row-major, contiguous.
- *   k_cache      [num_pages, P, Hkv, 192] of bf16 or E4M3 bytes.
+ *   q            bf16 [total_q, Hq, Dqk], row-major, contiguous (Dqk = the
+ *                plan's head_dim_qk: 192 or 128).
+ *   k_cache      [num_pages, P, Hkv, Dqk] of bf16 or E4M3 bytes.
  *   v_cache      [num_pages, P, Hkv, 128] of the same type.
  *   page_table   int32 [B, page_table_stride]; entries at or beyond
  *                ceil(seq_lens[b] / P) are never read, and with a window
@@ -213,7 +220,7 @@ attn_status_t attn_run_phase(attn_plan_t plan, int32_t phase, const void *q,
  *                how an FP8 E4M3 KV cache with a per-tensor scale stores its
  *                entries (model card MiMo-V2.6-Flash-RL-FP8KV-W4A8-2x-RTX-PRO-
  *                6000, "What the kernels do"); V likewise with v_scale.
- *   k_new, v_new bf16 [total_q][Hkv][192] and [total_q][Hkv][128], contiguous.
+ *   k_new, v_new bf16 [total_q][Hkv][Dqk] and [total_q][Hkv][128], contiguous.
  *   k_cache, v_cache, page_table, seq_lens, qo_indptr: as for attn_run_paged
  *                (device copies equal to the plan's host arrays).
  *   k_scale, v_scale  finite and > 0 for FP8 caches; ignored for BF16.

@@ -45,8 +45,10 @@ def _problem(**kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(head_dim_qk=128), B.ATTN_ERR_UNSUPPORTED),
+    (dict(head_dim_qk=64), B.ATTN_ERR_UNSUPPORTED),
+    (dict(head_dim_qk=256), B.ATTN_ERR_UNSUPPORTED),
     (dict(head_dim_v=192), B.ATTN_ERR_UNSUPPORTED),
+    (dict(head_dim_qk=128, head_dim_v=64), B.ATTN_ERR_UNSUPPORTED),
     (dict(num_q_heads=15), B.ATTN_ERR_UNSUPPORTED),
     (dict(seq_lens=[100, 5]), B.ATTN_ERR_INVALID_ARG),          # L < n
     (dict(qo_indptr=[0, 3, 2]), B.ATTN_ERR_INVALID_ARG),        # non-monotone
@@ -211,6 +213,23 @@ def test_named_configs_schedule_shape():
         info = B.attn_plan_info(plan)
         assert info["rows_per_block"] == rows, name
         assert 0 < info["ctas"] <= 152
+
+
+def test_symmetric_head_dim_pair_is_planned_without_the_prefill_kernel():
+    # 128/128 (a layer with a symmetric pair of its own) is accepted; its large
+    # blocks stay at 128 rows, since the 256-row prefill kernel is built for
+    # 192/128 only
+    for seq, n, hq, hkv, rows in [([46008] * 4, [8] * 4, 16, 2, 64),
+                                  ([30096], [4096], 64, 4, 128)]:
+        for dqk, want in [(128, rows), (192, 256 if n[0] > 8 else rows)]:
+            prob, keep = B.make_problem(batch=len(seq), num_q_heads=hq, num_kv_heads=hkv,
+                                        page_size=128, num_pages=9375,
+                                        page_table_stride=max((s + 127) // 128 for s in seq),
+                                        kv_dtype=0, window=0, has_sinks=False,
+                                        qo_indptr=np.concatenate([[0], np.cumsum(n)]),
+                                        seq_lens=seq, head_dim_qk=dqk, head_dim_v=128)
+            info = B.attn_plan_info(B.attn_plan_host(prob, 152, keep))
+            assert info["rows_per_block"] == want, (dqk, seq)
 
 
 def test_small_blocks_are_not_split_when_ctas_suffice():

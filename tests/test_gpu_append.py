@@ -11,19 +11,22 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # name, seq_lens, n, hq, hkv, P, kv
-    ("decode_p128", [1000, 129, 3000], [1, 1, 1], 16, 2, 128, "bf16"),
-    ("verify_p16", [700, 40], [8, 8], 16, 2, 16, "bf16"),
-    ("prefill_p1", [300], [120], 8, 1, 1, "bf16"),
-    ("ragged_empty", [90, 50, 20], [5, 0, 3], 8, 2, 3, "bf16"),
-    ("fp8_verify_p128", [900, 300], [8, 3], 16, 2, 128, "fp8"),
-    ("fp8_prefill_p3", [260], [200], 16, 4, 3, "fp8"),
+    # name, seq_lens, n, hq, hkv, P, kv, query/key head dim
+    ("decode_p128", [1000, 129, 3000], [1, 1, 1], 16, 2, 128, "bf16", 192),
+    ("verify_p16", [700, 40], [8, 8], 16, 2, 16, "bf16", 192),
+    ("prefill_p1", [300], [120], 8, 1, 1, "bf16", 192),
+    ("ragged_empty", [90, 50, 20], [5, 0, 3], 8, 2, 3, "bf16", 192),
+    ("fp8_verify_p128", [900, 300], [8, 3], 16, 2, 128, "fp8", 192),
+    ("fp8_prefill_p3", [260], [200], 16, 4, 3, "fp8", 192),
+    # a layer with the symmetric pair 128/128
+    ("sym_verify_p16", [700, 40], [8, 8], 16, 2, 16, "bf16", 128),
+    ("sym_fp8_prefill_p3", [260], [200], 16, 4, 3, "fp8", 128),
 ]
 
 
-def _new_rows(seed, total_q, hkv):
+def _new_rows(seed, total_q, hkv, dqk=192):
     rng = np.random.default_rng(seed)
-    k = (rng.standard_normal((total_q, hkv, 192)) * 2).astype(np.float32)
+    k = (rng.standard_normal((total_q, hkv, dqk)) * 2).astype(np.float32)
     v = (rng.standard_normal((total_q, hkv, 128)) * 2).astype(np.float32)
     return W.bf16_bits(k), W.bf16_bits(v)
 
@@ -32,10 +35,10 @@ def _new_rows(seed, total_q, hkv):
 def test_append_bit_exact(case):
     from asymmetric_kv_paged_gb300 import binding as B
     from asymmetric_kv_paged_gb300.runner import DeviceWorkload
-    name, seq, n, hq, hkv, P, kv = case
-    w = W.make_workload(17, seq, n, hq=hq, hkv=hkv, page_size=P, kv_dtype=kv, name=name)
+    name, seq, n, hq, hkv, P, kv, dqk = case
+    w = W.make_workload(17, seq, n, hq=hq, hkv=hkv, page_size=P, kv_dtype=kv, name=name, dqk=dqk)
     dw = DeviceWorkload(w)
-    kn, vn = _new_rows(23, w.total_q, hkv)
+    kn, vn = _new_rows(23, w.total_q, hkv, dqk)
     ks, vs = (w.k_scale, w.v_scale) if kv == "fp8" else (1.0, 1.0)
     ref_k, ref_v, skipped = A.append_kv(kn, vn, w.k_cache, w.v_cache, w.page_table, w.seq_lens,
                                         w.qo_indptr, kv, ks, vs)

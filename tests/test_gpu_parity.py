@@ -99,6 +99,23 @@ def test_parity_small(case):
     run_and_check(w)
 
 
+# Layers with the symmetric pair 128/128 (a model whose SWA layers carry a
+# head-dim pair of their own: sglang PR #32818, "Three changes", item 1).
+# Blocks of more than 128 rows run on the split-KV kernel at M = 128.
+SYM = ["decode_ragged_p128", "decode_ragged_p3", "verify_p1", "verify_p128", "swa_sinks_mixed",
+       "swa_small_window", "prefill_g16", "empty_requests", "fp8_decode", "fp8_verify_sinks",
+       "fp8_prefill", "fp8_swa", "fp8_prefill_p3_gather"]
+
+
+@pytest.mark.parametrize("name", SYM)
+def test_parity_symmetric_head_dims(name):
+    _, seq, n, hq, hkv, P, win, sinks, kv = next(c for c in SMALL if c[0] == name)
+    w = W.make_workload(zlib.crc32(name.encode()) % 1000 + 7, seq, n, hq=hq, hkv=hkv, page_size=P,
+                        window=win, sinks=sinks, kv_dtype=kv, name="sym_" + name, dqk=128)
+    assert w.q.shape[2] == 128 and w.k_cache.shape[3] == 128
+    run_and_check(w)
+
+
 @pytest.mark.parametrize("P", [1, 16, 128])
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_v_path_bit_exact(P, kv):
