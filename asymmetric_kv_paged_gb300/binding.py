@@ -22,7 +22,8 @@ ATTN_KV_FP8_E4M3 = 1
 
 EXPORTED = ("attn_plan", "attn_run_paged", "attn_run_phase", "attn_plan_destroy", "attn_get_device_error",
             "attn_status_string", "attn_plan_host", "attn_plan_info", "attn_plan_blocks",
-            "attn_plan_segments", "attn_debug_tc_gemm", "attn_run_paged_no_workspace",
+            "attn_plan_segments", "attn_plan_cta_heads", "attn_debug_tc_gemm",
+            "attn_run_paged_no_workspace",
             "attn_append_kv", "attn_plan_replayable", "attn_plan_replayable_host",
             "attn_plan_replan_host", "attn_plan_fetch_device")
 
@@ -285,6 +286,17 @@ def attn_plan_segments(plan: Plan):
     _check(load().attn_plan_segments(ctypes.c_void_p(plan.handle),
                                      arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
            "attn_plan_segments")
+    return arr[:n]
+
+
+def attn_plan_cta_heads(plan: Plan):
+    """Each CTA's head record as 20 int32 (see attn_plan_cta_heads)."""
+    import numpy as np
+    n = attn_plan_info(plan)["ctas"]
+    arr = np.zeros((max(n, 1), 20), np.int32)
+    _check(load().attn_plan_cta_heads(ctypes.c_void_p(plan.handle),
+                                      arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+           "attn_plan_cta_heads")
     return arr[:n]
 
 

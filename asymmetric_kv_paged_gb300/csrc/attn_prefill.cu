@@ -83,17 +83,22 @@ struct Cursor {
   int seg, seg_end, tile, si;
   SegDesc sd;
   BlockDesc bd;
-  __device__ void init(const SegDesc *s, const BlockDesc *b, int first, int end) {
+  __device__ void init(const SegDesc *s, const BlockDesc *b, const CtaHead &h) {
     segs = s;
     blocks = b;
-    seg = first;
-    seg_end = end;
+    seg = h.seg_begin;
+    seg_end = h.seg_end;
     si = 0;
-    load();
+    sd = h.seg;       // the first segment and its block come with the head record
+    bd = h.blk;
+    pin_all();
   }
   __device__ void load() {
     sd = segs[seg];
     bd = blocks[sd.block];
+    pin_all();
+  }
+  __device__ void pin_all() {
     // keep every field in a register (see attn_tc.cu: re-reads from global
     // memory would sit behind the K/V traffic)
     pin(sd.block); pin(sd.tile_begin); pin(sd.tile_end); pin(sd.split);
@@ -167,11 +172,12 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArg
   // the split merge (a programmatic dependent) may be scheduled now; it waits
   // for this grid's completion before it reads anything written here
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  const int seg_begin = a.cta_seg_begin[blockIdx.x];
-  const int seg_end = a.cta_seg_begin[blockIdx.x + 1];
+  // the CTA's head record: segment range, tile count, first segment and block
+  const CtaHead head = a.cta_heads[blockIdx.x];
+  const int seg_begin = head.seg_begin;
+  const int seg_end = head.seg_end;
   if (seg_begin >= seg_end) return;
-  int total = 0;
-  for (int s = seg_begin; s < seg_end; ++s) total += a.segs[s].tile_end - a.segs[s].tile_begin;
+  const int total = head.total;
 
   if (tid == 0) {
     abort_flag = 0;
@@ -489,7 +495,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArg
       const uint32_t s_tmem = tmem + kPN * t;
       const uint32_t o_tmem = tmem + kTmemO + kDv * t;
       Cursor cm;
-      cm.init(a.segs, a.blocks, seg_begin, seg_end);
+      cm.init(a.segs, a.blocks, head);
       int ct = 0;      // key tiles with rows in this Q tile
       int segs_t = 0;  // finished segments with rows in this Q tile
       int n1 = 0;      // (thread 0) key tiles so far that had Q tile 1 rows

@@ -121,17 +121,22 @@ struct Cursor {
   int seg, seg_end, tile, si;
   SegDesc sd;
   BlockDesc bd;
-  __device__ void init(const SegDesc *s, const BlockDesc *b, int first, int end) {
+  __device__ void init(const SegDesc *s, const BlockDesc *b, const CtaHead &h) {
     segs = s;
     blocks = b;
-    seg = first;
-    seg_end = end;
+    seg = h.seg_begin;
+    seg_end = h.seg_end;
     si = 0;
-    load();
+    sd = h.seg;       // the first segment and its block come with the head record
+    bd = h.blk;
+    pin_all();
   }
   __device__ void load() {
     sd = segs[seg];
     bd = blocks[sd.block];
+    pin_all();
+  }
+  __device__ void pin_all() {
     // Pin every field in a register: without this the compiler may re-read a
     // field from global memory at each later use (it may assume the kernel's
     // float / bf16 stores cannot alias these ints), and under the K/V stream
@@ -188,9 +193,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-template <bool FP8, bool TMA, int MR, int DQK>
+// HALF (M = 64 only): every block of the plan has more than 32 rows, so each
+// row has one copy, and lanes l and l + 16 of a softmax warp share row
+// 16w + l % 16, each taking 32 of the tile's 64 key columns (the two-half
+// 16-lane TMEM shapes): every lane works, on half the columns.
+template <bool FP8, bool TMA, int MR, int DQK, bool HALF>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const RunArgs args, const __grid_constant__ TmaMaps maps) {
+  static_assert(!HALF || MR == 64, "two threads per row only with the M = 64 layout");
   // A plain local copy of the arguments: the role lambdas capture by reference,
   // and a reference into kernel-parameter space would turn every field read
   // inside them into a memory load that the K/V stream keeps evicting.
@@ -218,11 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // let a programmatic dependent (the split merge) be scheduled now; it
   // waits for this grid's completion before it reads anything written here
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  const int seg_begin = a.cta_seg_begin[blockIdx.x];
-  const int seg_end = a.cta_seg_begin[blockIdx.x + 1];
+  // the CTA's head record: segment range, tile count, first segment and block
+  const CtaHead head = a.cta_heads[blockIdx.x];
+  const int seg_begin = head.seg_begin;
+  const int seg_end = head.seg_end;
   if (seg_begin >= seg_end) return;
-  int total = 0;
-  for (int s = seg_begin; s < seg_end; ++s) total += a.segs[s].tile_end - a.segs[s].tile_begin;
+  const int total = head.total;
 
   if (tid == 0) {
     abort_flag = 0;
@@ -277,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ln = tid & 31;
       int64_t *ring = reinterpret_cast<int64_t *>(smem + Lay::kOffSlots);
       Cursor cur;
-      cur.init(a.segs, a.blocks, seg_begin, seg_end);
+      cur.init(a.segs, a.blocks, head);
       bool ok = true;
       for (int k0 = 0; k0 < total && ok; k0 += kBatchTiles) {
         int64_t sl[kBatchTiles][2];
@@ -321,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int oob = a.num_pages * a.page_size;              // first slot past the pool
       constexpr uint32_t kTileBytes = FP8 ? kRawBytes : kOpBytes;
       Cursor cur;
-      cur.init(a.segs, a.blocks, seg_begin, seg_end);
+      cur.init(a.segs, a.blocks, head);
       for (int k = 0; k < total; ++k, cur.next()) {
         const int t = k % NT;
         const BlockDesc &bd = cur.bd;
@@ -375,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t *kc = static_cast<const uint8_t *>(a.k_cache);
     const uint8_t *vc = static_cast<const uint8_t *>(a.v_cache);
     Cursor cur;
-    cur.init(a.segs, a.blocks, seg_begin, seg_end);
+    cur.init(a.segs, a.blocks, head);
     // Stage the Q rows of the cursor's segment (row position p holds block
     // row p % rows_pad).  The loads go out 8-12 at a time: under a saturated
     // K/V stream each round trip to memory takes microseconds.
@@ -581,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((tid & 31) == 0) {
       const uint32_t id_s = tc::idesc_f16(1, 0, 0, kRows, kN);
       Cursor cs;
-      cs.init(a.segs, a.blocks, seg_begin, seg_end);
+      cs.init(a.segs, a.blocks, head);
       // BF16 + TMA: interior tiles are consumed straight off the TMA barrier;
       // edge tiles wait for the converters, whose barrier then completes only
       // on edge tiles (one parity bit per stage).
@@ -629,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((tid & 31) == 0) {
       const uint32_t id_pv = tc::idesc_f16(1, 0, 1, kRows, kDv);
       Cursor cp;
-      cp.init(a.segs, a.blocks, seg_begin, seg_end);
+      cp.init(a.segs, a.blocks, head);
       for (int kp = 0; kp < total; ++kp, cp.next()) {
         const int b = kp & 1;
         const int s = kp % NS;
@@ -664,10 +675,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // MMA row position held in this thread's TMEM lane: with M = 128 row p is
     // lane p; with M = 64 rows 16w..16w+15 sit in lanes 0-15 of warp w's
     // subpartition and lanes 16-31 hold no row (pos = -1).
-    const int pos = kRows == 128 ? t : (lane < 16 ? warp * 16 + lane : -1);
+    const int pos = kRows == 128 ? t : (HALF || lane < 16 ? warp * 16 + (lane & 15) : -1);
+    const int half = HALF ? lane >> 4 : 0;   // which 32 of the row's 64 columns
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     Cursor cur;
-    cur.init(a.segs, a.blocks, seg_begin, seg_end);
+    cur.init(a.segs, a.blocks, head);
     float m_run = -INFINITY, l_run = 0.f;
     int row_lo = 0, row_hi = 0, rr = 0, rows_pad = kRows, col0 = 0, off = 0, len = kN, nc = kN;
     int zero_pending = 0;
@@ -736,7 +748,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The TMEM loads are warp-collective: the whole warp takes the max pass
       // when any of its rows needs it, and only those rows adopt its result.
       const bool want_max = valid && (cur.first() || m_run == -INFINITY);
-      if (__any_sync(0xffffffffu, want_max)) {
+      if (HALF && __any_sync(0xffffffffu, want_max)) {
+        uint32_t r[32];
+        tc::tmem_ld_16x32bx2_x32<32>(taddr, r);
+        tc::tmem_wait_ld_regs32(r);
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int jj = 32 * half + j;
+          const float x0 = (jj >= j_lo) & (jj < j_hi) ? __uint_as_float(r[j]) : -INFINITY;
+          const float x1 = (jj + 1 >= j_lo) & (jj + 1 < j_hi) ? __uint_as_float(r[j + 1]) : -INFINITY;
+          mx[(j >> 1) & 1] = tc::max3(mx[(j >> 1) & 1], x0, x1);
+        }
+        float m = fmaxf(mx[0], mx[1]);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if (want_max) m_run = m * sc;
+      } else if (!HALF && __any_sync(0xffffffffu, want_max)) {
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
@@ -790,20 +817,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           rs[i] = 0.f;
           mx[i] = -INFINITY;
         }
-        tc::tmem_ld16(taddr, ra);
-        tc::tmem_wait_ld_regs(ra);
+        if constexpr (HALF) {
+          // this thread's 32 columns in one TMEM round trip; P goes back as 16
+          // pairs, the halves 16 pair columns apart
+          uint32_t r[32];
+          tc::tmem_ld_16x32bx2_x32<32>(taddr, r);
+          tc::tmem_wait_ld_regs32(r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int jj = 32 * half + j;
+            float x0 = __uint_as_float(r[j]), x1 = __uint_as_float(r[j + 1]);
+            if (!full) {
+              x0 = (jj >= j_lo) & (jj < j_hi) ? x0 : -INFINITY;
+              x1 = (jj + 1 >= j_lo) & (jj + 1 < j_hi) ? x1 : -INFINITY;
+            }
+            mx[(j >> 1) & 3] = tc::max3(mx[(j >> 1) & 3], x0, x1);
+            float y0, y1;
+            tc::ffma2(y0, y1, x0, x1, sc, neg_m);
+            const float p0 = ex2(y0), p1 = ex2(y1);
+            if (j & 2)
+              tc::fadd2(rs[2], rs[3], p0, p1);
+            else
+              tc::fadd2(rs[0], rs[1], p0, p1);
+            pk[j / 2] = cvt_pair(p0, p1);
+          }
+          tc::tmem_st_16x32bx2_x16<16>(pcol, pk);
+        } else {
+          tc::tmem_ld16(taddr, ra);
+          tc::tmem_wait_ld_regs(ra);
 #pragma unroll 1
-        for (int c = 0; c < nch; c += 2) {
-          if (c + 1 < nch) tc::tmem_ld16(taddr + 16 * (c + 1), rb);
-          exp16(ra, c, neg_m);
-          if (c + 1 < nch) {
-            tc::tmem_wait_ld_regs(rb);
-            if (c + 2 < nch) tc::tmem_ld16(taddr + 16 * (c + 2), ra);
-            exp16(rb, c + 1, neg_m);
-            if (c + 2 < nch) tc::tmem_wait_ld_regs(ra);
+          for (int c = 0; c < nch; c += 2) {
+            if (c + 1 < nch) tc::tmem_ld16(taddr + 16 * (c + 1), rb);
+            exp16(ra, c, neg_m);
+            if (c + 1 < nch) {
+              tc::tmem_wait_ld_regs(rb);
+              if (c + 2 < nch) tc::tmem_ld16(taddr + 16 * (c + 2), ra);
+              exp16(rb, c + 1, neg_m);
+              if (c + 2 < nch) tc::tmem_wait_ld_regs(ra);
+            }
           }
         }
-        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+        float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+        // the two halves of a row agree on its tile maximum
+        if (HALF) m_tile = fmaxf(m_tile, __shfl_xor_sync(0xffffffffu, m_tile, 16));
         const bool need = m_tile > m_run + kRescaleThreshold;
         if (pass > 0 || !__any_sync(0xffffffffu, need)) break;
         // rare: the maximum grew past the threshold; rescale O and redo
@@ -834,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < total; ++k, cur.next()) {
       const BlockDesc &bd = cur.bd;
       if (cur.first()) {
-        rows_pad = rows_pad_of(bd.nrows);
+        rows_pad = HALF ? kRows : rows_pad_of(bd.nrows);   // HALF plans: one copy per row
         rr = pos >= 0 ? pos % rows_pad : 0;
         valid = pos >= 0 && rr < bd.nrows;
         // copy c = pos / rows_pad of a row owns key columns [c*len, (c+1)*len) of
@@ -878,6 +935,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---------------- end of segment: normalise and write the block's rows
       if (!wait(&bars.pv_done[b], (k >> 1) & 1)) break;
+      if constexpr (HALF) {
+        // the row's two halves: one denominator; the lower half writes the row
+        // (its lane holds the row's O)
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
+        valid = valid && half == 0;
+      }
       tc::tc_fence_after();
       const SegDesc &sd = cur.sd;
       const bool single = bd.num_splits == 1;
@@ -1035,35 +1098,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool FP8, bool TMA, int MR, int DQK>
+template <bool FP8, bool TMA, int MR, int DQK, bool HALF>
 cudaError_t launch_one(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
-  attn_tc_kernel<FP8, TMA, MR, DQK>
+  attn_tc_kernel<FP8, TMA, MR, DQK, HALF>
       <<<hp.num_ctas, kThreads, Layout<FP8, MR, TMA, DQK>::kSmem, st>>>(a, m);
   return cudaGetLastError();
 }
 
-template <bool FP8, bool TMA, int MR, int DQK>
+template <bool FP8, bool TMA, int MR, int DQK, bool HALF>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(attn_tc_kernel<FP8, TMA, MR, DQK>,
+  return cudaFuncSetAttribute(attn_tc_kernel<FP8, TMA, MR, DQK, HALF>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Layout<FP8, MR, TMA, DQK>::kSmem);
 }
 
-template <int MR, int DQK>
+template <int MR, int DQK, bool HALF>
 cudaError_t launch_rows(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
   const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
   if (hp.use_tma)
-    return fp8 ? launch_one<true, true, MR, DQK>(hp, a, m, st)
-               : launch_one<false, true, MR, DQK>(hp, a, m, st);
-  return fp8 ? launch_one<true, false, MR, DQK>(hp, a, m, st)
-             : launch_one<false, false, MR, DQK>(hp, a, m, st);
+    return fp8 ? launch_one<true, true, MR, DQK, HALF>(hp, a, m, st)
+               : launch_one<false, true, MR, DQK, HALF>(hp, a, m, st);
+  return fp8 ? launch_one<true, false, MR, DQK, HALF>(hp, a, m, st)
+             : launch_one<false, false, MR, DQK, HALF>(hp, a, m, st);
 }
 
-template <int MR, int DQK>
+template <int MR, int DQK, bool HALF>
 cudaError_t prepare_rows(const HostPlan &hp) {
   const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
-  if (hp.use_tma) return fp8 ? prepare_one<true, true, MR, DQK>() : prepare_one<false, true, MR, DQK>();
-  return fp8 ? prepare_one<true, false, MR, DQK>() : prepare_one<false, false, MR, DQK>();
+  if (hp.use_tma)
+    return fp8 ? prepare_one<true, true, MR, DQK, HALF>() : prepare_one<false, true, MR, DQK, HALF>();
+  return fp8 ? prepare_one<true, false, MR, DQK, HALF>() : prepare_one<false, false, MR, DQK, HALF>();
+}
+
+// M = 64 plans whose blocks all have more than 32 rows run the two-threads-
+// per-row instantiation.
+template <int DQK>
+cudaError_t launch_dqk(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
+  if (hp.block_rows != 64) return launch_rows<128, DQK, false>(hp, a, m, st);
+  return hp.one_copy ? launch_rows<64, DQK, true>(hp, a, m, st)
+                     : launch_rows<64, DQK, false>(hp, a, m, st);
+}
+
+template <int DQK>
+cudaError_t prepare_dqk(const HostPlan &hp) {
+  if (hp.block_rows != 64) return prepare_rows<128, DQK, false>(hp);
+  return hp.one_copy ? prepare_rows<64, DQK, true>(hp) : prepare_rows<64, DQK, false>(hp);
 }
 
 }  // namespace
@@ -1076,17 +1155,12 @@ bool tc_tma_page_size(int32_t page_size, int32_t num_pages) {
 cudaError_t launch_attn_tc(const HostPlan &hp, const RunArgs &a, const TmaMaps &m,
                            cudaStream_t stream) {
   if (hp.num_ctas == 0) return cudaSuccess;
-  if (hp.prob.head_dim_qk == kDqkSym)
-    return hp.block_rows == 64 ? launch_rows<64, 128>(hp, a, m, stream)
-                               : launch_rows<128, 128>(hp, a, m, stream);
-  return hp.block_rows == 64 ? launch_rows<64, kDqk>(hp, a, m, stream)
-                             : launch_rows<128, kDqk>(hp, a, m, stream);
+  return hp.prob.head_dim_qk == kDqkSym ? launch_dqk<kDqkSym>(hp, a, m, stream)
+                                        : launch_dqk<kDqk>(hp, a, m, stream);
 }
 
 cudaError_t prepare_attn_tc(const HostPlan &hp) {
-  if (hp.prob.head_dim_qk == kDqkSym)
-    return hp.block_rows == 64 ? prepare_rows<64, 128>(hp) : prepare_rows<128, 128>(hp);
-  return hp.block_rows == 64 ? prepare_rows<64, kDqk>(hp) : prepare_rows<128, kDqk>(hp);
+  return hp.prob.head_dim_qk == kDqkSym ? prepare_dqk<kDqkSym>(hp) : prepare_dqk<kDqk>(hp);
 }
 
 }  // namespace akp

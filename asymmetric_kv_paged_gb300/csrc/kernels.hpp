@@ -22,6 +22,7 @@ struct RunArgs {
   const BlockDesc *blocks;
   const SegDesc *segs;
   const int32_t *cta_seg_begin;
+  const CtaHead *cta_heads;
   const MergeItem *merge_items;
   int32_t hq, hkv, group, page_size, pt_stride, num_pages, window;
   int32_t *err;

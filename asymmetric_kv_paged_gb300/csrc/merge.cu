@@ -22,11 +22,55 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Fold splits [0, S) of one row into (M, Z, acc), kB splits per step (see
+// merge_kernel).
+template <int kB>
+__device__ __forceinline__ void combine(const RunArgs &a, int base, int nrows, int S, int lane,
+                                        float &M, float &Z, float4 &acc) {
+  for (int s0 = 0; s0 < S; s0 += kB) {
+    float ls[kB];
+    float4 v[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      ls[u] = -INFINITY;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 + u < S) {      // no load at all for splits past the row's last
+        const int prow = base + (s0 + u) * nrows;
+        ls[u] = __ldcg(a.part_lse + prow);
+        v[u] = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (int64_t)prow * kDv) + lane);
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int u = 0; u < kB; ++u) Mn = fmaxf(Mn, ls[u]);
+    if (Mn == -INFINITY) continue;          // nothing seen yet
+    if (M != -INFINITY) {
+      const float c = exp2f(M - Mn);
+      Z *= c;
+      acc.x *= c;
+      acc.y *= c;
+      acc.z *= c;
+      acc.w *= c;
+    }
+    M = Mn;
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      if (ls[u] == -INFINITY) continue;
+      const float w = exp2f(ls[u] - M);
+      Z += w;
+      acc.x += w * v[u].x;
+      acc.y += w * v[u].y;
+      acc.z += w * v[u].z;
+      acc.w += w * v[u].w;
+    }
+  }
+}
+
 // Launched as a programmatic dependent of the attention kernel: everything
 // that kernel does not write (the item, the block, the sink) is read before
 // griddepcontrol.wait, so that part overlaps the attention kernel's tail; the
 // partials are read after it, all splits' loads issued before any is used.
-__global__ void __launch_bounds__(32 * kMergeRowsPerCta) merge_kernel(const RunArgs a) {
+__global__ void __launch_bounds__(32 * kMergeRowsPerCta, 3) merge_kernel(const RunArgs a) {
   const MergeItem it = a.merge_items[blockIdx.x];
   const BlockDesc bd = a.blocks[it.block];
   if (bd.num_splits <= 1) return;   // a replayable plan's run left the block whole
@@ -42,35 +86,21 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerCta) merge_kernel(const RunA
   if (!live) return;
   const int S = bd.num_splits;
   const int base = bd.part_row_base + r;
-  float M = sig;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(a.part_lse + base + s * bd.nrows));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  // One pass over the splits against a running maximum M (base 2), kB splits
+  // per step with all their loads issued before any is used: every step is
+  // one round trip to L2 (the maximum is not taken in a pass of its own).  The
+  // sink enters as a split with no value row.  Rows of at most 4 splits (the
+  // usual case) take a 4-wide step, longer ones (verify blocks cut over many
+  // CTAs) an 8-wide one; the register count stays low enough for three CTAs of
+  // eight warps per SM.
+  float M = sig, Z = sig == -INFINITY ? 0.f : 1.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float Z = 0.f, lse = -INFINITY;
+  if (S <= 4)
+    combine<4>(a, base, bd.nrows, S, lane, M, Z, acc);
+  else
+    combine<8>(a, base, bd.nrows, S, lane, M, Z, acc);
+  float lse = -INFINITY;
   if (M != -INFINITY) {
-    Z = exp2f(sig - M);
-    // four splits per step: their loads are independent and go out together
-    for (int s0 = 0; s0 < S; s0 += 4) {
-      float ls[4];
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int prow = base + min(s0 + u, S - 1) * bd.nrows;
-        ls[u] = __ldcg(a.part_lse + prow);
-        v[u] = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (int64_t)prow * kDv) + lane);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (s0 + u >= S || ls[u] == -INFINITY) continue;
-        const float w = exp2f(ls[u] - M);
-        Z += w;
-        acc.x += w * v[u].x;
-        acc.y += w * v[u].y;
-        acc.z += w * v[u].z;
-        acc.w += w * v[u].w;
-      }
-    }
     const float inv = 1.f / Z;
     acc.x *= inv;
     acc.y *= inv;

@@ -36,6 +36,16 @@ struct SegDesc {
   int32_t block, tile_begin, tile_end, split;
 };
 
+// What a CTA reads first: its segment range, its key-tile count, and its
+// first segment with that segment's block, in one 80-byte record, so that the
+// kernel's start costs one memory round trip instead of three dependent ones.
+struct CtaHead {
+  int32_t seg_begin, seg_end, total, pad;
+  SegDesc seg;
+  BlockDesc blk;
+};
+static_assert(sizeof(CtaHead) == 80, "CtaHead layout");
+
 // One merge item: rows [row_begin, row_begin + 8) of a multi-split block.
 struct MergeItem {
   int32_t block, row_begin;
@@ -49,11 +59,13 @@ struct HostPlan {
   int32_t block_rows = 128;      // 64 or 128 (the MMA M), or 256 (prefill kernel)
   int32_t key_tile = kKeyTile;   // keys per tile: 64, or 128 for the prefill kernel
   bool prefill = false;          // block_rows == 256: attn_prefill.cu runs the plan
+  bool one_copy = false;         // every block has more than block_rows / 2 rows
   int32_t num_sms = 0, num_ctas = 0, threads = 0;
   std::vector<BlockDesc> blocks;
   std::vector<SegDesc> segs;
   std::vector<int32_t> seg_cta;        // CTA of each segment
   std::vector<int32_t> cta_seg_begin;  // [num_ctas + 1]
+  std::vector<CtaHead> cta_heads;      // [num_ctas]
   std::vector<MergeItem> merge_items;
   int64_t part_rows = 0;
   size_t workspace_bytes = 0;
@@ -71,6 +83,7 @@ struct DevicePlan {
   BlockDesc *blocks = nullptr;
   SegDesc *segs = nullptr;
   int32_t *cta_seg_begin = nullptr;
+  CtaHead *cta_heads = nullptr;
   MergeItem *merge_items = nullptr;
   int32_t *err = nullptr;  // device error word
   // replayable plans only

@@ -18,6 +18,15 @@
 
 namespace akp {
 
+namespace {
+void fill_cta_heads(HostPlan *hp) {
+  hp->cta_heads.resize(hp->num_ctas);
+  for (int32_t c = 0; c < hp->num_ctas; ++c)
+    hp->cta_heads[c] = cta_head(hp->segs.data(), hp->blocks.data(), hp->cta_seg_begin[c],
+                                hp->cta_seg_begin[c + 1]);
+}
+}  // namespace
+
 
 attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan *out) {
   if (!p || !out || num_sms <= 0) return ATTN_ERR_INVALID_ARG;
@@ -102,6 +111,11 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
     }
   }
 
+  // Blocks of more than half the MMA rows hold one copy of each row; on M = 64
+  // the split-KV kernel then runs two threads per row (verify blocks).
+  hp.one_copy = !hp.blocks.empty();
+  for (const BlockDesc &bd : hp.blocks) hp.one_copy = hp.one_copy && 2 * bd.nrows > rows_per_block;
+
   // Deal tiles to CTAs in block order, cutting a block where a CTA's share
   // ends.  Each new CTA's share is the remaining tiles over the remaining
   // CTAs, so rounding never piles up on the last one; a block remainder of at
@@ -169,6 +183,7 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   }
   if (hp.part_rows > INT32_MAX / kDv) return ATTN_ERR_UNSUPPORTED;
   hp.workspace_bytes = hp.part_rows ? part_o_bytes(hp.part_rows) + part_lse_bytes(hp.part_rows) : 0;
+  fill_cta_heads(&hp);
   *out = std::move(hp);
   return ATTN_OK;
 }
@@ -254,6 +269,7 @@ int32_t replan_host(HostPlan *hp, const int32_t *seq_lens) {
       hp->multi_split_blocks++;
     }
   }
+  fill_cta_heads(hp);
   return err;
 }
 

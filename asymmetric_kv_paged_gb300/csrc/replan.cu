@@ -1,6 +1,7 @@
 // Device planner of replayable plans: before each attention launch, one CTA
 // reads the run's request lengths and rewrites the plan's work list (block
-// key ranges, segments, CTA segment ranges, splits and partial-row offsets)
+// key ranges, segments, CTA segment ranges, splits, partial-row offsets and
+// the CTAs' head records)
 // in place, so that a captured CUDA graph stays valid while requests grow.
 // The arithmetic is in replan.hpp, shared with the host mirror.
 #include <cuda_runtime.h>
@@ -111,6 +112,11 @@ __global__ void __launch_bounds__(kReplanThreads, 1) replan_kernel(const ReplanA
   cta_exclusive_scan(r.part_start, r.nb);
   for (int32_t bi = tid; bi < r.nb; bi += kReplanThreads)
     r.blocks[bi].part_row_base = r.blocks[bi].num_splits > 1 ? r.part_start[bi] : -1;
+  __syncthreads();
+
+  // each CTA's head record, from the final segments and blocks
+  for (int32_t c = tid; c < r.num_ctas; c += kReplanThreads)
+    r.cta_heads[c] = cta_head(r.segs, r.blocks, r.cta_seg_begin[c], r.cta_seg_begin[c + 1]);
 }
 
 }  // namespace

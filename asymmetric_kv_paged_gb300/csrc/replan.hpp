@@ -84,11 +84,25 @@ AKP_HD int32_t share_splits(int64_t gs, int64_t ge, int64_t T, int64_t ctas) {
   return share_owner(ge - 1, T, ctas) - share_owner(gs, T, ctas) + 1;
 }
 
+// The head record of a CTA whose segments are [s0, s1) (see CtaHead).
+AKP_HD CtaHead cta_head(const SegDesc *segs, const BlockDesc *blocks, int32_t s0, int32_t s1) {
+  CtaHead h{};
+  h.seg_begin = s0;
+  h.seg_end = s1;
+  for (int32_t s = s0; s < s1; ++s) h.total += segs[s].tile_end - segs[s].tile_begin;
+  if (s0 < s1) {
+    h.seg = segs[s0];
+    h.blk = blocks[h.seg.block];
+  }
+  return h;
+}
+
 // Arguments of the device planner (replan.cu).
 struct ReplanArgs {
   BlockDesc *blocks;           // [nb]; b, g, row0, nrows, n, tok0 fixed
   SegDesc *segs;               // capacity nb + num_ctas
   int32_t *cta_seg_begin;      // [num_ctas + 1]
+  CtaHead *cta_heads;          // [num_ctas]
   int32_t *tile_start;         // scratch [nb + 1]
   int32_t *part_start;         // scratch [nb + 1]
   const int32_t *seq_lens;     // [B] lengths of this run (caller's device array)

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (mode == 0) {
     stage_sw128(sa, a, 128, 192);   // [128 x 192] K-major
     stage_sw128(sb, b, n, 192);     // [n x 192] K-major
-  } else if (mode == 2 || mode == 5) {
+  } else if (mode == 2 || mode == 5 || mode == 6) {
     stage_sw128(sa, a, 64, 192);    // [64 x 192] K-major
     stage_sw128(sb, b, 64, 192);    // [64 x 192] K-major
   } else if (mode == 1) {
@@ -66,8 +66,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const int M = (mode == 2 || mode == 4 || mode == 5) ? 64 : 128;
-  if (mode >= 3) {
+  const int M = (mode == 2 || mode == 4 || mode == 5 || mode == 6) ? 64 : 128;
+  if (mode == 3 || mode == 4) {
     // A = P [M x 64] into TMEM columns 256..287, each thread its own row's
     // lane (M = 64: rows 16w..16w+15 in lanes 0-15 of warp w's quadrant)
     const int lane = threadIdx.x & 31;
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd = tc::smem_desc_sw128(b0 + (ks / 4) * n * 128 + koff, 16, 1024);
         tc::mma_f16_ss(tmem, ad, bd, idesc, ks > 0);
       }
-    } else if (mode == 2 || mode == 5) {
+    } else if (mode == 2 || mode == 5 || mode == 6) {
       const uint32_t idesc = tc::idesc_f16(ab_type, 0, 0, 64, 64);
       for (int ks = 0; ks < 12; ++ks) {
         const uint32_t koff = (ks % 4) * 32u;
@@ -123,7 +123,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const int ncols = mode == 0 ? n : (mode == 2 ? 64 : 128);
   (void)M;
-  if (ok && mode == 5) {
+  if (ok && mode == 6) {
+    // the two-half 16-lane shapes: a 16x32bx2.x32 load with the halves 32
+    // columns apart, dumped as d[warp][thread][register]; then a 16x32bx2.x16
+    // store at column 64 with the halves 16 columns apart, and a 32x32b load
+    // of columns 64-95 into d[4*32*32 + (warp*32 + lane)*32 + column]
+    const int t = threadIdx.x & 31;
+    uint32_t r[32];
+    tc::tmem_ld_16x32bx2_x32<32>(tmem + ((uint32_t)(warp * 32) << 16), r);
+    tc::tmem_wait_ld();
+    for (int j = 0; j < 32; ++j) d[(warp * 32 + t) * 32 + j] = __uint_as_float(r[j]);
+    uint32_t w16[16];
+    for (int j = 0; j < 16; ++j) w16[j] = (uint32_t)(warp * 100000 + t * 100 + j);
+    tc::tmem_st_16x32bx2_x16<16>(tmem + ((uint32_t)(warp * 32) << 16) + 64, w16);
+    tc::tmem_wait_st();
+    uint32_t q[32];
+    tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 64, q);
+    tc::tmem_wait_ld();
+    for (int j = 0; j < 32; ++j) d[4 * 32 * 32 + (warp * 32 + t) * 32 + j] = (float)q[j];
+  } else if (ok && mode == 5) {
     // the 16-lane shapes: every thread's 32 registers of a 16x256b.x8 load of
     // its warp's lanes 0-15, dumped as d[warp][thread][register]; then the
     // 16x128b.x8 store writes register pairs back (column 64 + ...) and a
@@ -163,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 extern "C" attn_status_t attn_debug_tc_gemm(int32_t mode, int32_t variant, int32_t ab_type,
                                             int32_t n, const void *a, const void *b, float *d,
                                             int32_t *status, void *stream) {
-  if (mode < 0 || mode > 5) return ATTN_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 6) return ATTN_ERR_INVALID_ARG;
   if (mode == 0 && n != 64 && n != 128) return ATTN_ERR_INVALID_ARG;
   if (variant != 0 && variant != 1) return ATTN_ERR_INVALID_ARG;
   if (ab_type != 0 && ab_type != 1) return ATTN_ERR_INVALID_ARG;

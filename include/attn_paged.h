@@ -321,6 +321,16 @@ attn_status_t attn_plan_host(const attn_problem_t *problem, int32_t num_sms, att
 attn_status_t attn_plan_info(attn_plan_t plan, int32_t info[8]);
 attn_status_t attn_plan_blocks(attn_plan_t plan, int32_t *blocks_host);
 attn_status_t attn_plan_segments(attn_plan_t plan, int32_t *segments_host);
+/*
+ * attn_plan_cta_heads copies each CTA's head record, the first thing a CTA of
+ * the attention kernels reads, as 20 int32 per CTA (info[2] CTAs):
+ *   {seg_begin, seg_end, key tiles in all its segments, 0,
+ *    its first segment {block, tile_begin, tile_end, split},
+ *    that segment's block {b, g, row0, nrows, L, n, tok0, key_lo, key_hi,
+ *    num_splits, part_row_base, 0}}
+ * (zeros after the range for a CTA without segments).  Errors: INVALID_ARG.
+ */
+attn_status_t attn_plan_cta_heads(attn_plan_t plan, int32_t *heads_host);
 attn_status_t attn_plan_replayable_host(const attn_problem_t *bounds, int32_t num_sms,
                                         attn_plan_t *plan);
 attn_status_t attn_plan_replan_host(attn_plan_t plan, const int32_t *seq_lens_host,

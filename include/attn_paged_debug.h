@@ -38,7 +38,14 @@ extern "C" {
  *           stores the values warp*100000 + thread*100 + j (j < 16) with a
  *           16x128b.x8 store at column 64, and d[4096 : 6144] receives a
  *           32x32b load of those 16 columns (index (warp*32 + lane)*16 + col)
- *           as floats.  d must hold 6144 floats.
+ *           as floats.  d must hold 6144 floats;
+ *   mode 6: the product of mode 2, then read back with the two-half shapes:
+ *           d[0 : 4096] = each thread's 32 registers of a 16x32bx2.x32 load
+ *           with the halves 32 columns apart; then every thread stores
+ *           warp*100000 + thread*100 + j (j < 16) with a 16x32bx2.x16 store at
+ *           column 64, halves 16 apart, and d[4096 : 8192] receives a 32x32b
+ *           load of columns 64-95 (index (warp*32 + lane)*32 + col) as
+ *           floats.  d must hold 8192 floats.
  * a, b: device 16-bit matrices, row-major (ab_type 0 = fp16, 1 = bf16);
  * d: device fp32, row-major; status: device int32, set to 1 if the
  * completion wait timed out (left untouched otherwise).  Asynchronous on

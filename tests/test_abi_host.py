@@ -178,6 +178,21 @@ def _check_plan(plan, w, num_sms):
     for cta, blk, t0, t1, split in segs:
         loads[cta] += t1 - t0
     assert loads.max() <= int(np.ceil(loads.sum() / info["ctas"])) * 1.25 + 2
+    # each CTA's head record (what the kernels read first): its segment range,
+    # its tile count, its first segment and that segment's block
+    heads = B.attn_plan_cta_heads(plan)
+    assert heads.shape == (info["ctas"], 20)
+    for c in range(info["ctas"]):
+        mine = np.nonzero(segs[:, 0] == c)[0]
+        h = heads[c]
+        if len(mine) == 0:
+            assert h[0] == h[1] and h[2] == 0
+            continue
+        assert h[0] == mine[0] and h[1] == mine[-1] + 1
+        assert h[2] == int((segs[mine, 3] - segs[mine, 2]).sum())
+        assert list(h[4:8]) == list(segs[mine[0], 1:5])
+        bi = segs[mine[0], 1]
+        assert list(h[8:12]) == list(blocks[bi, :4]) and list(h[15:19]) == list(blocks[bi, 4:8])
     return info
 
 

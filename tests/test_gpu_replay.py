@@ -92,6 +92,7 @@ def test_graph_replay_with_changing_lengths(case):
         assert B.attn_plan_replan_host(mirror, lens) == 0
         assert np.array_equal(B.attn_plan_blocks(dw.plan), B.attn_plan_blocks(mirror))
         assert np.array_equal(B.attn_plan_segments(dw.plan), B.attn_plan_segments(mirror))
+        assert np.array_equal(B.attn_plan_cta_heads(dw.plan), B.attn_plan_cta_heads(mirror))
 
 
 def test_lengths_outside_bounds_are_clamped_and_flagged():

@@ -126,3 +126,34 @@ def test_sixteen_lane_tmem_shapes():
                 h, tr = divmod(lane, 8)
                 t = 4 * tr + tq
                 assert stv[w, lane, col] == float(w * 100000 + t * 100 + 2 * i + h), (w, lane, col)
+
+
+def test_two_half_sixteen_lane_tmem_shapes():
+    """The 16x32bx2 TMEM access shapes on an M=64 accumulator: threads t < 16
+    of warp w see row 16w + t at columns [0, 32), threads t >= 16 the same row
+    16w + t - 16 at the split offset (columns [32, 64)); the store puts thread
+    t's registers in row 16w + t % 16 at columns 64 + 16 (t // 16) + j."""
+    import numpy as np
+    g = torch.Generator(device="cuda").manual_seed(12)
+    a = torch.randn(64, 192, device="cuda", generator=g).to(torch.bfloat16)
+    b = torch.randn(64, 192, device="cuda", generator=g).to(torch.bfloat16)
+    from asymmetric_kv_paged_gb300 import binding as B
+    d = torch.zeros(8192, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.attn_debug_tc_gemm(6, 0, 1, 64, a, b, d, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = (a.float() @ b.float().T).cpu().numpy()
+    got = d.cpu().numpy()
+    ld = got[:4096].reshape(4, 32, 32)
+    tol = 1e-3 * np.abs(ref).max()
+    for w in range(4):
+        for t in range(32):
+            row, c0 = 16 * w + t % 16, 32 * (t // 16)
+            assert np.all(np.abs(ld[w, t] - ref[row, c0:c0 + 32]) < tol), (w, t)
+    stv = got[4096:].reshape(4, 32, 32)
+    for w in range(4):
+        for lane in range(16):
+            for col in range(32):
+                t = lane + 16 * (col // 16)
+                assert stv[w, lane, col] == float(w * 100000 + t * 100 + col % 16), (w, lane, col)
