@@ -123,11 +123,16 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   // becoming a split of its own.
   const int64_t nb = (int64_t)hp.blocks.size();
   constexpr int64_t kWholeBlockTiles = 8;
+  // A CTA that goes on to a further segment pays for the switch (the finished
+  // segment's epilogue, the next block's Q) with this many tiles of its share:
+  // measured, two-segment CTAs otherwise ended ~3-5 us after the others.
+  constexpr int64_t kSegSwitchTiles = 3;
   if (nb > 0) {
     const int64_t min_tiles = 2;
     int64_t remaining = total_tiles;
     int32_t cta = -1;
     int64_t room = 0, target = 0, slack = 0;
+    bool charge = false;          // this CTA's share pays for its segment switches
     for (int64_t bi = 0; bi < nb; ++bi) {
       BlockDesc &bd = hp.blocks[bi];
       int32_t t0 = bd.klo / tile;
@@ -138,6 +143,13 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
           ++cta;
           const int64_t ctas_left = std::max<int64_t>(1, (int64_t)num_sms - cta);
           target = std::max<int64_t>(min_tiles, (remaining + ctas_left - 1) / ctas_left);
+          // Large shares count the switches still ahead (about one per block
+          // not yet begun) as work, so that the CTAs after a switch are not
+          // left with the tiles the switching ones gave up; shares of a few
+          // tiles, where most CTAs switch, stay even in tiles.
+          charge = cta + 1 < num_sms && target >= 8 * kSegSwitchTiles;
+          if (charge)
+            target = (remaining + kSegSwitchTiles * (nb - bi - 1) + ctas_left - 1) / ctas_left;
           slack = target / 32;
           room = target;
         }
@@ -158,6 +170,8 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
         hp.segs.push_back(s);
         hp.seg_cta.push_back(cta);
         room -= take;
+        // the CTA's next tiles start a new segment (the last CTA takes all that is left)
+        if (room > 0 && charge) room -= kSegSwitchTiles;
         remaining -= take;
         t0 += (int32_t)take;
       }
