@@ -88,6 +88,11 @@ SMALL = [
     # gathered (page sizes TMA cannot tile) with blocks of more than 64 rows: M = 128
     ("prefill_p1_gather", [600], [100], 8, 1, 1, 0, True, "bf16"),
     ("fp8_prefill_p3_gather", [500, 90], [80, 3], 16, 2, 3, 0, False, "fp8"),
+    # every block of 33-64 rows: M = 64 with two threads per row; partly filled
+    # blocks, a window with sinks, and one block cut over many CTAs
+    ("verify_half_40rows", [900, 700], [5, 5], 16, 2, 16, 0, True, "bf16"),
+    ("verify_half_swa_fp8", [3000, 2500], [8, 6], 16, 2, 128, 100, True, "fp8"),
+    ("verify_half_split", [20000], [8], 16, 2, 128, 0, False, "bf16"),
 ]
 
 
@@ -102,7 +107,8 @@ def test_parity_small(case):
 # Layers with the symmetric pair 128/128 (a model whose SWA layers carry a
 # head-dim pair of their own: sglang PR #32818, "Three changes", item 1).
 # Blocks of more than 128 rows run on the split-KV kernel at M = 128.
-SYM = ["decode_ragged_p128", "decode_ragged_p3", "verify_p1", "verify_p128", "swa_sinks_mixed",
+SYM = ["decode_ragged_p128", "decode_ragged_p3", "verify_p1", "verify_p128", "verify_half_split",
+       "swa_sinks_mixed",
        "swa_small_window", "prefill_g16", "empty_requests", "fp8_decode", "fp8_verify_sinks",
        "fp8_prefill", "fp8_swa", "fp8_prefill_p3_gather"]
 
