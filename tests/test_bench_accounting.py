@@ -14,7 +14,7 @@ from asymmetric_kv_paged_gb300 import workloads as W
 ROW = 192 + 128
 
 
-def shape(name, seq, n, hq, hkv, P, window=0, kv="bf16", sinks=False):
+def shape(name, seq, n, hq, hkv, P, window=0, kv="bf16", sinks=False, dqk=192):
     seq = np.asarray(seq, np.int32)
     n = np.asarray(n, np.int64)
     qo = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
@@ -23,7 +23,7 @@ def shape(name, seq, n, hq, hkv, P, window=0, kv="bf16", sinks=False):
                       kv_dtype=kv, qo_indptr=qo, seq_lens=seq,
                       page_table=np.zeros((len(seq), 1), np.int32), q=empty, k_cache=empty,
                       v_cache=empty, sinks=np.zeros(hq, np.float32) if sinks else None,
-                      softmax_scale=1.0)
+                      softmax_scale=1.0, dqk=dqk)
 
 
 def test_tiny_decode():
@@ -61,6 +61,19 @@ def test_swa_with_sinks():
     assert bench.algorithmic_bytes(w) == kv + q_out + table + 16 * 4 == 13_722_048
     # every row sees exactly 128 keys (all positions are past the window)
     assert bench.algorithmic_flops(w) == 2 * ROW * (32 + 256) * 16 * 128
+
+
+def test_swa_with_sinks_symmetric_head_dims():
+    # the same batch on a layer whose pair is 128/128: 256 bytes per K row
+    n = [1, 8] * 32
+    w = shape("c4s", [8192] * 64, n, 16, 2, 128, window=128, sinks=True, dqk=128)
+    row = 128 + 128
+    keys = 32 * 128 + 32 * 135
+    kv = keys * 2 * row * 2
+    q_out = (32 * 1 + 32 * 8) * 16 * row * 2
+    table = (32 * 1 + 32 * 2) * 4
+    assert bench.algorithmic_bytes(w) == kv + q_out + table + 16 * 4 == 10_977_728
+    assert bench.algorithmic_flops(w) == 2 * row * (32 + 256) * 16 * 128
 
 
 def test_chunked_prefill():

@@ -402,9 +402,10 @@ def whole_blocks_to_check(w, plan, count=16):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", list(W.CONFIG_NAMES))
+@pytest.mark.parametrize("name", list(W.CONFIG_NAMES) + list(W.EXTRA_NAMES))
 def test_parity_named_config(name):
-    """Every output row of the decode, verify and SWA workloads at full size, and
+    """Every output row of the decode, verify and SWA workloads (the 128/128 SWA
+    shape included) at full size, and
     at least 16 whole row blocks of the prefill chunk (first and last block of
     every KV head and blocks split over several CTAs), each against the oracle."""
     w = W.named(name)
