@@ -169,8 +169,13 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArg
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  // the split merge (a programmatic dependent) may be scheduled now; it waits
-  // for this grid's completion before it reads anything written here
+  // Launched as a programmatic dependent (of the device planner or the KV
+  // append, when they precede it): nothing they write is read before this wait.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // The split merge (a programmatic dependent of this kernel) may be scheduled
+  // from here on: it reads the plan's blocks before its own wait, so only once
+  // the planner that writes them has completed; it waits for this grid's
+  // completion before it reads anything written here.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   // the CTA's head record: segment range, tile count, first segment and block
   const CtaHead head = a.cta_heads[blockIdx.x];
@@ -824,10 +829,10 @@ done:
 cudaError_t launch_attn_prefill(const HostPlan &hp, const RunArgs &a, cudaStream_t stream) {
   if (hp.num_ctas == 0) return cudaSuccess;
   if (hp.prob.kv_dtype == ATTN_KV_FP8_E4M3)
-    attn_prefill_kernel<true><<<hp.num_ctas, kPThreads, kSmem, stream>>>(a);
-  else
-    attn_prefill_kernel<false><<<hp.num_ctas, kPThreads, kSmem, stream>>>(a);
-  return cudaGetLastError();
+    return launch_dependent(attn_prefill_kernel<true>, dim3(hp.num_ctas), dim3(kPThreads), kSmem,
+                            stream, a);
+  return launch_dependent(attn_prefill_kernel<false>, dim3(hp.num_ctas), dim3(kPThreads), kSmem,
+                          stream, a);
 }
 
 cudaError_t prepare_attn_prefill(const HostPlan &hp) {

@@ -225,8 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  // let a programmatic dependent (the split merge) be scheduled now; it
-  // waits for this grid's completion before it reads anything written here
+  // Launched as a programmatic dependent (of the device planner or the KV
+  // append, when they precede it): nothing they write is read before this wait.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // The split merge (a programmatic dependent of this kernel) may be scheduled
+  // from here on: it reads the plan's blocks before its own wait, so only once
+  // the planner that writes them has completed; it waits for this grid's
+  // completion before it reads anything written here.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   // the CTA's head record: segment range, tile count, first segment and block
   const CtaHead head = a.cta_heads[blockIdx.x];
@@ -1100,9 +1105,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool FP8, bool TMA, int MR, int DQK, bool HALF>
 cudaError_t launch_one(const HostPlan &hp, const RunArgs &a, const TmaMaps &m, cudaStream_t st) {
-  attn_tc_kernel<FP8, TMA, MR, DQK, HALF>
-      <<<hp.num_ctas, kThreads, Layout<FP8, MR, TMA, DQK>::kSmem, st>>>(a, m);
-  return cudaGetLastError();
+  return launch_dependent(attn_tc_kernel<FP8, TMA, MR, DQK, HALF>, dim3(hp.num_ctas),
+                          dim3(kThreads), Layout<FP8, MR, TMA, DQK>::kSmem, st, a, m);
 }
 
 template <bool FP8, bool TMA, int MR, int DQK, bool HALF>

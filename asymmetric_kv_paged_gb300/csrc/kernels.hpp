@@ -28,6 +28,26 @@ struct RunArgs {
   int32_t *err;
 };
 
+// Launch `kernel` as a programmatic dependent of the stream's previous kernel:
+// its CTAs may be scheduled while that kernel finishes (the launch latency is
+// hidden), and the kernel itself waits (griddepcontrol.wait) before it reads
+// anything an earlier kernel of the stream writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Tensor maps of the K and V caches as 3D tensors [slots][Hkv][D] (TMA loads).
 struct TmaMaps {
   CUtensorMap k, v;

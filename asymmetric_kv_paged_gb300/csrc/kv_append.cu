@@ -47,6 +47,9 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
 
 template <bool FP8>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+  // the kernels that follow in a serving step (device planner, attention) may
+  // be scheduled now; they wait for this grid before reading the caches
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < a.units;
        u += (int64_t)gridDim.x * blockDim.x) {
     const int chunks = a.k_chunks + kVChunks;

@@ -73,7 +73,6 @@ __device__ __forceinline__ void combine(const RunArgs &a, int base, int nrows, i
 __global__ void __launch_bounds__(32 * kMergeRowsPerCta, 3) merge_kernel(const RunArgs a) {
   const MergeItem it = a.merge_items[blockIdx.x];
   const BlockDesc bd = a.blocks[it.block];
-  if (bd.num_splits <= 1) return;   // a replayable plan's run left the block whole
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int r = it.row_begin + warp;
@@ -82,8 +81,10 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerCta, 3) merge_kernel(const R
   const int tok = bd.tok0 + flat / a.group;
   const int h = bd.g * a.group + flat % a.group;
   const float sig = (a.sinks && live) ? a.sinks[h] * kLog2e : -INFINITY;
+  // Every CTA waits, also those with nothing to do: this grid's completion
+  // then implies the attention kernel's, for a dependent launched after it.
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  if (!live) return;
+  if (bd.num_splits <= 1 || !live) return;   // a replayable plan's run may leave the block whole
   const int S = bd.num_splits;
   const int base = bd.part_row_base + r;
   // One pass over the splits against a running maximum M (base 2), kB splits

@@ -57,6 +57,13 @@ __device__ void cta_exclusive_scan(int32_t *v, int32_t n) {
 
 __global__ void __launch_bounds__(kReplanThreads, 1) replan_kernel(const ReplanArgs r) {
   const int tid = threadIdx.x;
+  // Launched as a programmatic dependent: the previous kernels of the stream
+  // (the last run's attention and merge, or the KV append) have completed once
+  // this wait returns, so the work list they read may be rewritten.  The
+  // attention kernel that follows may be scheduled now; it waits for this
+  // grid to complete.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   // lengths (clamped into [n_b, bound_b]) and key ranges of every block
   for (int32_t bi = tid; bi < r.nb; bi += kReplanThreads) {
@@ -123,8 +130,7 @@ __global__ void __launch_bounds__(kReplanThreads, 1) replan_kernel(const ReplanA
 
 cudaError_t launch_replan(const ReplanArgs &r, cudaStream_t stream) {
   if (r.nb == 0) return cudaSuccess;
-  replan_kernel<<<1, kReplanThreads, 0, stream>>>(r);
-  return cudaGetLastError();
+  return launch_dependent(replan_kernel, dim3(1), dim3(kReplanThreads), 0, stream, r);
 }
 
 }  // namespace akp
