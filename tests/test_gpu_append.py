@@ -95,3 +95,42 @@ def test_append_out_of_pool_page_sets_error_word():
     torch.cuda.synchronize()
     assert B.attn_get_device_error(dw.plan) & 1
     assert torch.equal(dw.k_cache.view(torch.int16), before_k.view(torch.int16))
+
+
+def test_serving_steps_append_then_replayed_attention():
+    """Three decode serving steps on one replayable plan, back to back on one
+    stream: each appends the new token's K/V rows (lengths grown by one) and
+    runs attention (device planner, attention kernel, merge, launched as
+    programmatic dependents).  Every step's output matches the attention oracle
+    on the oracle-appended cache."""
+    import bench
+    from asymmetric_kv_paged_gb300 import binding as B
+    from asymmetric_kv_paged_gb300.runner import DeviceWorkload
+    from oracle import oracle
+    w = W.make_workload(43, [700, 300, 1000, 65], [1, 1, 1, 1], hq=16, hkv=2, page_size=16,
+                        kv_dtype="bf16", sinks=True, name="serving_steps")
+    steps = 3
+    g = bench.grown_workload(w, steps)
+    dw = DeviceWorkload(g, replayable=True)
+    L0 = w.seq_lens.astype(np.int32)
+    kc, vc = g.k_cache, g.v_cache
+    outs, refs = [], []
+    for s in range(steps):
+        lens = L0 + 1 + s                       # the new token sits at position L0 + s
+        kn, vn = _new_rows(50 + s, w.total_q, w.hkv)
+        kc, vc, skipped = A.append_kv(kn, vn, kc, vc, g.page_table, lens, w.qo_indptr, "bf16")
+        assert skipped == 0
+        dw.seq_lens.copy_(torch.from_numpy(lens))
+        B.attn_append_kv(dw.plan, torch.from_numpy(kn).view(torch.bfloat16).cuda(),
+                         torch.from_numpy(vn).view(torch.bfloat16).cuda(), dw.k_cache, dw.v_cache,
+                         dw.page_table, dw.seq_lens, dw.qo_indptr, 1.0, 1.0)
+        dw.run()
+        outs.append(dw.out.float().clone())
+        pb = g.host_arrays()
+        pb["k_cache"], pb["v_cache"], pb["seq_lens"] = kc, vc, lens
+        refs.append(oracle.attn_paged(pb)[0])
+    torch.cuda.synchronize()
+    assert B.attn_get_device_error(dw.plan) == 0
+    for s in range(steps):
+        err = np.abs(outs[s].cpu().numpy() - refs[s])
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3, (s, err.max(), err.mean())
