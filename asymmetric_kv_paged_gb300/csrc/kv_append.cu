@@ -35,6 +35,7 @@ struct AppendArgs {
   int64_t units;            // total_q * hkv * (k_chunks + 16)
   int32_t batch, hkv, page_size, pt_stride, num_pages;
   int32_t dqk, k_chunks;    // query/key head dim, 16-byte chunks of a K row (dqk / 8)
+  int32_t qo_in_smem;       // nonzero: the launch gives (batch + 1) * 4 bytes of shared memory
   float k_scale, v_scale;
 };
 
@@ -50,6 +51,15 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   // the kernels that follow in a serving step (device planner, attention) may
   // be scheduled now; they wait for this grid before reading the caches
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  // qo_indptr in shared memory when it fits (the launch passes the size): the
+  // request of a token is then found without a chain of dependent global loads
+  extern __shared__ int32_t s_qo[];
+  const bool qo_smem = a.qo_in_smem != 0;
+  if (qo_smem) {
+    for (int i = threadIdx.x; i <= a.batch; i += blockDim.x) s_qo[i] = __ldg(a.qo_indptr + i);
+    __syncthreads();
+  }
+  auto qo_at = [&](int i) { return qo_smem ? s_qo[i] : __ldg(a.qo_indptr + i); };
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < a.units;
        u += (int64_t)gridDim.x * blockDim.x) {
     const int chunks = a.k_chunks + kVChunks;
@@ -57,14 +67,20 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     const int64_t pair = u / chunks;
     const int g = (int)(pair % a.hkv);
     const int tok = (int)(pair / a.hkv);
+    // the source chunk depends on nothing that follows: its load goes out first
+    const bool is_k = chunk < a.k_chunks;
+    const int c = is_k ? chunk : chunk - a.k_chunks;
+    const int D = is_k ? a.dqk : kDv;
+    const uint4 src = __ldg(reinterpret_cast<const uint4 *>((is_k ? a.k_new : a.v_new) +
+                                                            ((int64_t)tok * a.hkv + g) * D) + c);
     // request of this token: last b with qo_indptr[b] <= tok
     int lo = 0, hi = a.batch - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(a.qo_indptr + mid) <= tok) lo = mid; else hi = mid - 1;
+      if (qo_at(mid) <= tok) lo = mid; else hi = mid - 1;
     }
     const int b = lo;
-    const int q0 = __ldg(a.qo_indptr + b), n = __ldg(a.qo_indptr + b + 1) - q0;
+    const int q0 = qo_at(b), n = qo_at(b + 1) - q0;
     const int64_t i = (int64_t)__ldg(a.seq_lens + b) - n + (tok - q0);
     if (i < 0 || i / a.page_size >= a.pt_stride) {   // a length outside the table row
       atomicOr(a.err, 4);
@@ -76,11 +92,6 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
       continue;
     }
     const int64_t slot = (int64_t)page * a.page_size + i % a.page_size;
-    const bool is_k = chunk < a.k_chunks;
-    const int c = is_k ? chunk : chunk - a.k_chunks;
-    const int D = is_k ? a.dqk : kDv;
-    const uint4 src = __ldg(reinterpret_cast<const uint4 *>((is_k ? a.k_new : a.v_new) +
-                                                            ((int64_t)tok * a.hkv + g) * D) + c);
     const int64_t row = (slot * a.hkv + g) * D;
     if (!FP8) {
       reinterpret_cast<uint4 *>(static_cast<uint16_t *>(is_k ? a.k_cache : a.v_cache) + row)[c] =
@@ -147,10 +158,13 @@ extern "C" attn_status_t attn_append_kv(attn_plan_t plan, const void *k_new, con
   const int64_t want = (a.units + 255) / 256;
   const unsigned grid = (unsigned)(want < 152 * 16 ? want : 152 * 16);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t qo_bytes = (size_t)(pr.batch + 1) * sizeof(int32_t);
+  a.qo_in_smem = qo_bytes <= 16 * 1024;
+  const size_t smem = a.qo_in_smem ? qo_bytes : 0;
   if (fp8)
-    akp::append_kernel<true><<<grid, 256, 0, st>>>(a);
+    akp::append_kernel<true><<<grid, 256, smem, st>>>(a);
   else
-    akp::append_kernel<false><<<grid, 256, 0, st>>>(a);
+    akp::append_kernel<false><<<grid, 256, smem, st>>>(a);
   const cudaError_t e = cudaGetLastError();
   if (prev != plan->device) cudaSetDevice(prev);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
