@@ -1,5 +1,6 @@
-// Split-KV paged attention on the Blackwell tensor-core path (tcgen05 + TMEM),
-// for every mode: decode, multi-token verify and chunked prefill.
+// Split-KV paged attention on the Blackwell tensor-core path (tcgen05 + TMEM)
+// for row blocks of up to 128 query rows: decode, multi-token verify, and
+// prefill chunks small enough (larger ones run attn_prefill.cu).
 //
 // A CTA walks the key tiles (64 keys) of its work segments.  Each segment
 // belongs to one row block: up to 128 query rows of one (request, KV head),
@@ -13,7 +14,9 @@
 //
 // Warp roles (352 threads):
 //   warps 0-3  softmax + epilogue: MMA row p lives in TMEM lane p (M=128) or
-//              in lane 32*(p/16) + p%16 (M=64), and that lane's thread owns it;
+//              in lane 32*(p/16) + p%16 (M=64), and that lane's thread owns it
+//              (HALF instantiations: lanes l and l+16 share row 16w + l%16,
+//              32 key columns each);
 //   warps 4-7  converters: stage Q per block; turn raw FP8 K/V tiles into
 //              exact bf16 operand tiles; zero V rows of keys outside the
 //              block's range on edge tiles (unused slots may hold NaN:
@@ -25,6 +28,8 @@
 //              operand layout; FP8: raw rows into a staging ring); for the
 //              gather path, the page lookups into a ring of resolved slots;
 //   warp 10    issues the O += P.V MMAs (one thread).
+// A CTA starts from its head record (segment range, tile count, first segment
+// and block) and is launched as a programmatic dependent (griddepcontrol).
 // TMEM: S double buffer (2 x 64 columns), O (128 columns), P double buffer (2 x 32).
 // Every wait is bounded in time; a broken invariant ends the kernel with bit 1
 // of the plan's error word set instead of hanging the GPU.
