@@ -436,3 +436,39 @@ def test_batch_without_query_rows():
     dw.run()
     torch.cuda.synchronize()
     assert B.attn_get_device_error(dw.plan) == 0
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_parity_random_shapes(seed):
+    """Seeded random problems, every output row against the oracle: ragged
+    lengths and query counts (decode, verify, short and long prefill blocks, so
+    M = 64 with and without two threads per row, M = 128 and the 256-row
+    prefill kernel), page sizes 1 / 3 / 16 / 64 / 128, windows, sinks, GQA
+    ratios, BF16 and FP8 caches, and both head-dim pairs."""
+    rng = np.random.default_rng(5000 + seed)
+    batch = int(rng.integers(1, 6))
+    hkv = int(rng.choice([1, 2]))
+    hq = hkv * int(rng.choice([1, 4, 8, 16]))
+    P = int(rng.choice([1, 3, 16, 64, 128]))
+    kind = rng.choice(["decode", "verify", "verify_wide", "prefill"])
+    if kind == "decode":
+        n = np.ones(batch, np.int64)
+    elif kind == "verify":
+        n = rng.integers(1, 9, batch)
+    elif kind == "verify_wide":          # blocks of 40-64 rows: two threads per row
+        hq = 8 * hkv
+        n = rng.integers(5, 9, batch)
+    else:
+        n = rng.integers(1, 300, batch)
+    n[rng.random(batch) < 0.2] = 0
+    seq = n + rng.integers(0, 1500, batch)
+    seq = np.maximum(seq, 1)
+    win = int(rng.choice([0, 0, 0, 7, 100]))
+    kv = str(rng.choice(["bf16", "fp8"]))
+    dqk = int(rng.choice([192, 192, 128]))
+    w = W.make_workload(seed, seq.tolist(), n.tolist(), hq=hq, hkv=hkv, page_size=P, window=win,
+                        sinks=bool(rng.random() < 0.5), kv_dtype=kv, dqk=dqk,
+                        name=f"random{seed}_{kind}_{kv}_p{P}_d{dqk}")
+    if w.total_q == 0:
+        pytest.skip("no query rows drawn")
+    run_and_check(w)
