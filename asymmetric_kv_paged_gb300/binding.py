@@ -22,7 +22,8 @@ ATTN_KV_FP8_E4M3 = 1
 
 EXPORTED = ("attn_plan", "attn_run_paged", "attn_run_phase", "attn_plan_destroy", "attn_get_device_error",
             "attn_status_string", "attn_plan_host", "attn_plan_info", "attn_plan_blocks",
-            "attn_plan_segments", "attn_plan_cta_heads", "attn_debug_tc_gemm",
+            "attn_plan_segments", "attn_plan_cta_heads", "attn_plan_stage_units",
+            "attn_debug_tc_gemm",
             "attn_run_paged_no_workspace",
             "attn_append_kv", "attn_plan_replayable", "attn_plan_replayable_host",
             "attn_plan_replan_host", "attn_plan_fetch_device")
@@ -298,6 +299,19 @@ def attn_plan_cta_heads(plan: Plan):
                                       arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
            "attn_plan_cta_heads")
     return arr[:n]
+
+
+def attn_plan_stage_units(plan: Plan):
+    """A prefill plan's staging units as 8 int32 each (see attn_plan_stage_units)."""
+    import numpy as np
+    n = ctypes.c_int32(0)
+    _check(load().attn_plan_stage_units(ctypes.c_void_p(plan.handle), ctypes.byref(n), None),
+           "attn_plan_stage_units")
+    arr = np.zeros((max(n.value, 1), 8), np.int32)
+    _check(load().attn_plan_stage_units(ctypes.c_void_p(plan.handle), ctypes.byref(n),
+                                        arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+           "attn_plan_stage_units")
+    return arr[:n.value]
 
 
 def attn_debug_tc_gemm(mode: int, variant: int, ab_type: int, n: int, a, b, d, status,

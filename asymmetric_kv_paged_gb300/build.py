@@ -20,6 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "attn_tc.cu", "attn_prefill.cu", "merge.cu", "replan.cu", "no_workspace.cu", "kv_append.cu",
+           "kv_stage.cu",
            "tc_selftest.cu", "planner.cpp"]
 HEADERS = ["plan.hpp", "replan.hpp", "kernels.hpp", "tc_common.cuh", "e4m3.cuh"]
 

@@ -68,6 +68,23 @@ bool make_cache_map(CUtensorMap *map, const void *base, bool fp8, int d, int hkv
   return r == CUDA_SUCCESS;
 }
 
+// Staging scratch of prefill plans (K: d = 192, V: d = 128 16-bit values a
+// row) as a 2D tensor [rows][d]: boxes of 64 columns x 128 rows (one key tile
+// of one 64-column operand block) with 128-byte swizzle.
+bool make_stage_map(CUtensorMap *map, const void *base, bool f16, int d, int64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)akp::kStageTile};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 void free_device(attn_plan_s *p) {
   if (p->dev.blocks) cudaFree(p->dev.blocks);
   p->dev = akp::DevicePlan{};
@@ -81,12 +98,13 @@ attn_status_t upload(attn_plan_s *p) {
   const size_t c_bytes = align256(hp.cta_seg_begin.size() * sizeof(int32_t));
   const size_t h_bytes = align256(hp.cta_heads.size() * sizeof(akp::CtaHead));
   const size_t m_bytes = align256(hp.merge_items.size() * sizeof(akp::MergeItem));
+  const size_t u_bytes = align256(hp.stage_units.size() * sizeof(akp::StageUnit));
   const size_t e_bytes = 256;
   // replayable plans: the length bounds and two scratch arrays of the planner
   const size_t r_bytes = hp.replayable ? align256(hp.seq_lens.size() * sizeof(int32_t)) +
                                              2 * align256((hp.blocks.size() + 1) * sizeof(int32_t))
                                        : 0;
-  const size_t total = b_bytes + s_bytes + c_bytes + m_bytes + e_bytes + r_bytes + h_bytes;
+  const size_t total = b_bytes + s_bytes + c_bytes + m_bytes + e_bytes + r_bytes + h_bytes + u_bytes;
   uint8_t *base = nullptr;
   if (cudaMalloc(&base, total) != cudaSuccess) return ATTN_ERR_CUDA;
   p->dev.blocks = reinterpret_cast<akp::BlockDesc *>(base);
@@ -96,6 +114,9 @@ attn_status_t upload(attn_plan_s *p) {
   p->dev.err = reinterpret_cast<int32_t *>(base + b_bytes + s_bytes + c_bytes + m_bytes);
   p->dev.cta_heads =
       reinterpret_cast<akp::CtaHead *>(base + b_bytes + s_bytes + c_bytes + m_bytes + e_bytes + r_bytes);
+  if (!hp.stage_units.empty())
+    p->dev.stage_units = reinterpret_cast<akp::StageUnit *>(base + b_bytes + s_bytes + c_bytes +
+                                                            m_bytes + e_bytes + r_bytes + h_bytes);
   if (hp.replayable) {
     uint8_t *r = base + b_bytes + s_bytes + c_bytes + m_bytes + e_bytes;
     p->dev.seq_bounds = reinterpret_cast<int32_t *>(r);
@@ -120,6 +141,9 @@ attn_status_t upload(attn_plan_s *p) {
   if (e == cudaSuccess && !hp.merge_items.empty())
     e = cudaMemcpy(p->dev.merge_items, hp.merge_items.data(),
                    hp.merge_items.size() * sizeof(akp::MergeItem), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && !hp.stage_units.empty())
+    e = cudaMemcpy(p->dev.stage_units, hp.stage_units.data(),
+                   hp.stage_units.size() * sizeof(akp::StageUnit), cudaMemcpyHostToDevice);
   if (e == cudaSuccess && hp.replayable && !hp.seq_lens.empty())
     e = cudaMemcpy(p->dev.seq_bounds, hp.seq_lens.data(), hp.seq_lens.size() * sizeof(int32_t),
                    cudaMemcpyHostToDevice);
@@ -208,7 +232,11 @@ attn_status_t attn_plan_destroy(attn_plan_t plan) {
   return ATTN_OK;
 }
 
-static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const void *k_cache,
+// allow_stage: a prefill plan's K/V staging scratch follows the partials in
+// the workspace; without it (the library-owned scratch of the no-workspace
+// entry point holds the partials only) the prefill kernel reads the caches.
+static attn_status_t run_impl(attn_plan_t plan, int phases, bool allow_stage, const void *q,
+                              const void *k_cache,
                               const void *v_cache, const int32_t *page_table,
                               const int32_t *seq_lens, const int32_t *qo_indptr,
                               const float *sinks, int32_t window, float softmax_scale,
@@ -227,8 +255,9 @@ static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const
   // the kernels take score maxima on unscaled dot products: the scale must be > 0
   if (!(softmax_scale > 0.f) || (pr.kv_dtype == ATTN_KV_FP8_E4M3 && !(k_scale > 0.f)))
     return ATTN_ERR_INVALID_ARG;
-  if (workspace_bytes < hp.workspace_bytes || (hp.workspace_bytes && !workspace))
-    return ATTN_ERR_WORKSPACE;
+  const bool staged = allow_stage && hp.stage_rows > 0;
+  const size_t need = staged ? hp.workspace_bytes : hp.partial_bytes;
+  if (workspace_bytes < need || (need && !workspace)) return ATTN_ERR_WORKSPACE;
   if (!has_rows) return ATTN_OK;
 
   const bool fp8 = pr.kv_dtype == ATTN_KV_FP8_E4M3;
@@ -293,8 +322,33 @@ static attn_status_t run_impl(attn_plan_t plan, int phases, const void *q, const
     r.key_tile = hp.key_tile;
     if (akp::launch_replan(r, st) != cudaSuccess) return ATTN_ERR_CUDA;
   }
+  akp::TmaMaps stage_maps{};
+  if ((phases & 1) && staged) {
+    uint8_t *ws = static_cast<uint8_t *>(workspace) + hp.partial_bytes;
+    akp::StageArgs sa{};
+    sa.units = plan->dev.stage_units;
+    sa.k_cache = k_cache;
+    sa.v_cache = v_cache;
+    sa.page_table = page_table;
+    sa.k_stage = reinterpret_cast<uint16_t *>(ws);
+    sa.v_stage = reinterpret_cast<uint16_t *>(ws + akp::stage_k_bytes(hp.stage_rows, pr.head_dim_qk));
+    sa.err = plan->dev.err;
+    sa.tiles = hp.stage_tiles;
+    sa.num_units = (int32_t)hp.stage_units.size();
+    sa.dqk = pr.head_dim_qk;
+    sa.hkv = pr.num_kv_heads;
+    sa.page_size = pr.page_size;
+    sa.pt_stride = pr.page_table_stride;
+    sa.num_pages = pr.num_pages;
+    sa.fp8 = fp8;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) ||
+        !make_stage_map(&stage_maps.k, sa.k_stage, fp8, pr.head_dim_qk, hp.stage_rows) ||
+        !make_stage_map(&stage_maps.v, sa.v_stage, fp8, akp::kDv, hp.stage_rows))
+      return ATTN_ERR_CUDA;
+    if (akp::launch_kv_stage(sa, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
   if (phases & 1) {
-    const cudaError_t le = hp.prefill ? akp::launch_attn_prefill(hp, a, st)
+    const cudaError_t le = hp.prefill ? akp::launch_attn_prefill(hp, a, staged ? &stage_maps : nullptr, st)
                                       : akp::launch_attn_tc(hp, a, maps, st);
     if (le != cudaSuccess) return ATTN_ERR_CUDA;
   }
@@ -308,7 +362,7 @@ attn_status_t attn_run_paged(attn_plan_t plan, const void *q, const void *k_cach
                              const float *sinks, int32_t window, float softmax_scale,
                              float k_scale, float v_scale, void *out, float *lse_out,
                              void *workspace, size_t workspace_bytes, void *stream) {
-  return run_impl(plan, 3, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks, window,
+  return run_impl(plan, 3, true, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks, window,
                   softmax_scale, k_scale, v_scale, out, lse_out, workspace, workspace_bytes,
                   stream);
 }
@@ -321,7 +375,7 @@ attn_status_t attn_run_phase(attn_plan_t plan, int32_t phase, const void *q,
                              float *lse_out, void *workspace, size_t workspace_bytes,
                              void *stream) {
   if (phase != 0 && phase != 1) return ATTN_ERR_INVALID_ARG;
-  return run_impl(plan, phase == 0 ? 1 : 2, q, k_cache, v_cache, page_table, seq_lens,
+  return run_impl(plan, phase == 0 ? 1 : 2, true, q, k_cache, v_cache, page_table, seq_lens,
                   qo_indptr, sinks, window, softmax_scale, k_scale, v_scale, out, lse_out,
                   workspace, workspace_bytes, stream);
 }
@@ -430,6 +484,14 @@ attn_status_t attn_plan_cta_heads(attn_plan_t plan, int32_t *heads_host) {
   return ATTN_OK;
 }
 
+attn_status_t attn_plan_stage_units(attn_plan_t plan, int32_t *count, int32_t *units_host) {
+  if (!plan || !count) return ATTN_ERR_INVALID_ARG;
+  const std::vector<akp::StageUnit> &u = plan->host.stage_units;
+  *count = (int32_t)u.size();
+  if (units_host && !u.empty()) std::memcpy(units_host, u.data(), u.size() * sizeof(akp::StageUnit));
+  return ATTN_OK;
+}
+
 attn_status_t attn_plan_segments(attn_plan_t plan, int32_t *segments_host) {
   if (!plan || (!segments_host && !plan->host.segs.empty())) return ATTN_ERR_INVALID_ARG;
   int32_t *d = segments_host;
@@ -443,3 +505,16 @@ attn_status_t attn_plan_segments(attn_plan_t plan, int32_t *segments_host) {
 }
 
 }  // extern "C"
+
+namespace akp {
+attn_status_t run_paged_unstaged(attn_plan_t plan, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *page_table,
+                                 const int32_t *seq_lens, const int32_t *qo_indptr,
+                                 const float *sinks, int32_t window, float softmax_scale,
+                                 float k_scale, float v_scale, void *out, float *lse_out,
+                                 void *workspace, size_t workspace_bytes, void *stream) {
+  return run_impl(plan, 3, false, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks,
+                  window, softmax_scale, k_scale, v_scale, out, lse_out, workspace,
+                  workspace_bytes, stream);
+}
+}  // namespace akp

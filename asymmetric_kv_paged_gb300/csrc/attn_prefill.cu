@@ -158,8 +158,13 @@ __device__ __forceinline__ int q_row_shift(const uint4 *row) {
   return min(141 - (int)e, 126);
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArgs args) {
+// STAGED: the K/V tiles are TMA boxes of the staging scratch (kv_stage.cu),
+// issued by one thread of the load warps; else the load warps read the paged
+// caches themselves (plans without a scratch: replayable plans, runs without
+// a workspace).
+template <bool FP8, bool STAGED>
+__global__ void __launch_bounds__(kPThreads, 1)
+    attn_prefill_kernel(const RunArgs args, const __grid_constant__ TmaMaps stage) {
   const RunArgs a = args;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
@@ -186,8 +191,10 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArg
 
   if (tid == 0) {
     abort_flag = 0;
+    // a K or V stage is filled by the four load warps, or by one TMA issue
+    constexpr uint32_t kFill = STAGED ? 1 : kLoadWarps;
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&bars.k_full[i], kLoadWarps);
+      tc::mbar_init(&bars.k_full[i], kFill);
       tc::mbar_init(&bars.k_empty[i], 2);
       tc::mbar_init(&bars.done[i], 1);
       tc::mbar_init(&bars.s_full[i], 1);
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArg
       tc::mbar_init(&bars.pv_done[i], 1);
       tc::mbar_init(&bars.o_free[i], 4);
     }
-    tc::mbar_init(&bars.v_full, kLoadWarps);
+    tc::mbar_init(&bars.v_full, kFill);
     tc::mbar_init(&bars.v_empty, 2);
     tc::mbar_init(&bars.q_full, kLoadWarps);
     tc::mbar_init(&bars.q_empty, 2);
@@ -368,118 +375,176 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_prefill_kernel(const RunArg
       return true;
     };
 
-    // The K stream runs one tile ahead of the V stream: iteration k stores
-    // K(k) (once Q.K^T of tile k-2 has freed its stage) and then V(k-1) (once
-    // P.V of tile k-2 is done), so a tile's K never waits behind the previous
-    // tile's P.V.  Page lookups run two tiles ahead of the K stream.
-    // Per tile in flight ([0]: tile k, [1]: k+1, [2]: k+2): its cache slot,
-    // and its KV head, segment and whether it starts the segment packed as
-    // segment << 17 | first << 16 | head.
-    KPos kp;
-    kpos_load(kp, seg_begin);
-    int64_t slot[3];
-    int info[3];
-    auto pack = [](int seg, bool first, int g) { return (seg << 17) | ((int)first << 16) | g; };
-    slot[0] = lookup(kp);
-    info[0] = pack(kp.seg, true, kp.g);
-    for (int i = 1; i < 3; ++i) {
-      slot[i] = -1;
-      info[i] = 0;
-      if (i < total) {
-        const int prev_seg = kp.seg;
-        kpos_next(kp);
-        slot[i] = lookup(kp);
-        info[i] = pack(kp.seg, kp.seg != prev_seg, kp.g);
+    if constexpr (STAGED) {
+      // K(k) and V(k-1) per iteration, as in the paths below, but as TMA
+      // boxes of the staging scratch (64 columns x 128 keys, 128-byte
+      // swizzle: the operand layout) issued by lane 0 of the first load warp;
+      // all four load warps stage the Q rows when a segment starts.  Key j of
+      // the block's (b, g) is scratch row srow + j.
+      const bool issuer = lt == 0;
+      int sg = seg_begin;
+      SegDesc ssd = head.seg;
+      int s_row = head.blk.srow;
+      int s_tile = ssd.tile_begin;
+      bool s_first = true;
+      int v_row = 0;
+      if (issuer) {
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&stage.k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&stage.v)) : "memory");
       }
-    }
-    auto shift = [&](int k) {    // tile k+1 becomes [0]; look up tile k+3 into [2]
-      slot[0] = slot[1];
-      info[0] = info[1];
-      slot[1] = slot[2];
-      info[1] = info[2];
-      slot[2] = -1;
-      if (k + 3 < total) {
-        const int prev_seg = kp.seg;
-        kpos_next(kp);
-        slot[2] = lookup(kp);
-        info[2] = pack(kp.seg, kp.seg != prev_seg, kp.g);
-      }
-    };
-    auto head_of = [](int in) { return in & 0xFFFF; };
-    auto starts = [](int in) { return ((in >> 16) & 1) != 0; };
-    auto seg_of = [](int in) { return in >> 17; };
-    if constexpr (FP8) {
-      // raw E4M3 rows in registers: K of tile k, V of tile k-1 (20 x 16 bytes)
-      constexpr int KCH = kDqk / 16, VCH = kDv / 16;
-      uint4 kr[KCH], vr[VCH];
-      int64_t v_slot = -1;
-      int v_g = 0;
-      load(kr, KCH, row_ptr(kc, slot[0], head_of(info[0]), kDqk), slot[0]);
       for (int k = 0; k <= total; ++k) {
+        bool ok = true;
         if (k < total) {
-          if (starts(info[0]) && !stage_q(seg_of(info[0]))) break;
-          const int s = k & 1;
-          if (k >= 2 && !tc::mbar_wait_warp(&bars.k_empty[s], ((k >> 1) - 1) & 1, &abort_flag)) break;
-          put_fp8(sbase + kOffK + s * kKStage, kr, KCH, false);
-          tc::fence_proxy_async_smem();
-          tc::mbar_arrive_warp(&bars.k_full[s]);
-          if (k + 1 < total) load(kr, KCH, row_ptr(kc, slot[1], head_of(info[1]), kDqk), slot[1]);
+          if (s_first && !stage_q(sg)) break;
+          if (issuer) {
+            const int s = k & 1;
+            ok = k < 2 || tc::mbar_wait(&bars.k_empty[s], ((k >> 1) - 1) & 1, &abort_flag);
+            if (ok) {
+              tc::mbar_arrive_expect_tx(&bars.k_full[s], kKStage);
+              const int y = s_row + s_tile * kPN;
+#pragma unroll
+              for (int c = 0; c < 3; ++c)
+                tc::tma_load_2d(sbase + kOffK + s * kKStage + c * kTileBlk, &stage.k, c * 64, y,
+                                &bars.k_full[s]);
+            }
+          }
         }
-        if (k >= 1) {
-          if (k >= 2 && !tc::mbar_wait_warp(&bars.v_empty, (k - 2) & 1, &abort_flag)) break;
-          put_fp8(sbase + kOffV, vr, VCH, false);
-          tc::fence_proxy_async_smem();
-          tc::mbar_arrive_warp(&bars.v_full);
+        if (k >= 1 && issuer && ok) {
+          ok = k < 2 || tc::mbar_wait(&bars.v_empty, (k - 2) & 1, &abort_flag);
+          if (ok) {
+            tc::mbar_arrive_expect_tx(&bars.v_full, kVStage);
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              tc::tma_load_2d(sbase + kOffV + c * kTileBlk, &stage.v, c * 64, v_row, &bars.v_full);
+          }
         }
+        if (__any_sync(0xffffffffu, !ok)) break;
         if (k < total) {
-          v_slot = slot[0];
-          v_g = head_of(info[0]);
-          load(vr, VCH, row_ptr(vc, v_slot, v_g, kDv), v_slot);
-          shift(k);
+          v_row = s_row + s_tile * kPN;
+          s_first = false;
+          if (++s_tile == ssd.tile_end && sg + 1 < seg_end) {
+            ++sg;
+            ssd = a.segs[sg];
+            s_row = a.blocks[ssd.block].srow;
+            s_tile = ssd.tile_begin;
+            s_first = true;
+          }
         }
       }
     } else {
-      // BF16 rows are twice as wide: each goes through registers in pieces of
-      // 12 and 8 chunks, loaded just before they are stored.
-      uint4 buf[12];
-      int64_t v_slot = -1;
-      int v_g = 0;
-      for (int k = 0; k <= total; ++k) {
-        if (k < total) {
-          if (starts(info[0]) && !stage_q(seg_of(info[0]))) break;
-          const uint4 *krow = row_ptr(kc, slot[0], head_of(info[0]), kDqk);
-          const int s = k & 1;
-          load(buf, 12, krow, slot[0]);
-          if (k >= 2 && !tc::mbar_wait_warp(&bars.k_empty[s], ((k >> 1) - 1) & 1, &abort_flag)) break;
-          const uint32_t kb = sbase + kOffK + s * kKStage;
-#pragma unroll
-          for (int i = 0; i < 12; ++i) put(kb, i, buf[i]);
-          load(buf, 12, krow + 12, slot[0]);
-#pragma unroll
-          for (int i = 0; i < 12; ++i) put(kb, 12 + i, buf[i]);
-          tc::fence_proxy_async_smem();
-          tc::mbar_arrive_warp(&bars.k_full[s]);
-        }
-        if (k >= 1) {
-          const uint4 *vrow = row_ptr(vc, v_slot, v_g, kDv);
-          load(buf, 8, vrow, v_slot);
-          if (k >= 2 && !tc::mbar_wait_warp(&bars.v_empty, (k - 2) & 1, &abort_flag)) break;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) put(sbase + kOffV, i, buf[i]);
-          load(buf, 8, vrow + 8, v_slot);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) put(sbase + kOffV, 8 + i, buf[i]);
-          tc::fence_proxy_async_smem();
-          tc::mbar_arrive_warp(&bars.v_full);
-        }
-        if (k < total) {
-          v_slot = slot[0];
-          v_g = head_of(info[0]);
-          shift(k);
+      // The K stream runs one tile ahead of the V stream: iteration k stores
+      // K(k) (once Q.K^T of tile k-2 has freed its stage) and then V(k-1) (once
+      // P.V of tile k-2 is done), so a tile's K never waits behind the previous
+      // tile's P.V.  Page lookups run two tiles ahead of the K stream.
+      // Per tile in flight ([0]: tile k, [1]: k+1, [2]: k+2): its cache slot,
+      // and its KV head, segment and whether it starts the segment packed as
+      // segment << 17 | first << 16 | head.
+      KPos kp;
+      kpos_load(kp, seg_begin);
+      int64_t slot[3];
+      int info[3];
+      auto pack = [](int seg, bool first, int g) { return (seg << 17) | ((int)first << 16) | g; };
+      slot[0] = lookup(kp);
+      info[0] = pack(kp.seg, true, kp.g);
+      for (int i = 1; i < 3; ++i) {
+        slot[i] = -1;
+        info[i] = 0;
+        if (i < total) {
+          const int prev_seg = kp.seg;
+          kpos_next(kp);
+          slot[i] = lookup(kp);
+          info[i] = pack(kp.seg, kp.seg != prev_seg, kp.g);
         }
       }
+      auto shift = [&](int k) {    // tile k+1 becomes [0]; look up tile k+3 into [2]
+        slot[0] = slot[1];
+        info[0] = info[1];
+        slot[1] = slot[2];
+        info[1] = info[2];
+        slot[2] = -1;
+        if (k + 3 < total) {
+          const int prev_seg = kp.seg;
+          kpos_next(kp);
+          slot[2] = lookup(kp);
+          info[2] = pack(kp.seg, kp.seg != prev_seg, kp.g);
+        }
+      };
+      auto head_of = [](int in) { return in & 0xFFFF; };
+      auto starts = [](int in) { return ((in >> 16) & 1) != 0; };
+      auto seg_of = [](int in) { return in >> 17; };
+      if constexpr (FP8) {
+        // raw E4M3 rows in registers: K of tile k, V of tile k-1 (20 x 16 bytes)
+        constexpr int KCH = kDqk / 16, VCH = kDv / 16;
+        uint4 kr[KCH], vr[VCH];
+        int64_t v_slot = -1;
+        int v_g = 0;
+        load(kr, KCH, row_ptr(kc, slot[0], head_of(info[0]), kDqk), slot[0]);
+        for (int k = 0; k <= total; ++k) {
+          if (k < total) {
+            if (starts(info[0]) && !stage_q(seg_of(info[0]))) break;
+            const int s = k & 1;
+            if (k >= 2 && !tc::mbar_wait_warp(&bars.k_empty[s], ((k >> 1) - 1) & 1, &abort_flag)) break;
+            put_fp8(sbase + kOffK + s * kKStage, kr, KCH, false);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive_warp(&bars.k_full[s]);
+            if (k + 1 < total) load(kr, KCH, row_ptr(kc, slot[1], head_of(info[1]), kDqk), slot[1]);
+          }
+          if (k >= 1) {
+            if (k >= 2 && !tc::mbar_wait_warp(&bars.v_empty, (k - 2) & 1, &abort_flag)) break;
+            put_fp8(sbase + kOffV, vr, VCH, false);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive_warp(&bars.v_full);
+          }
+          if (k < total) {
+            v_slot = slot[0];
+            v_g = head_of(info[0]);
+            load(vr, VCH, row_ptr(vc, v_slot, v_g, kDv), v_slot);
+            shift(k);
+          }
+        }
+      } else {
+        // BF16 rows are twice as wide: each goes through registers in pieces of
+        // 12 and 8 chunks, loaded just before they are stored.
+        uint4 buf[12];
+        int64_t v_slot = -1;
+        int v_g = 0;
+        for (int k = 0; k <= total; ++k) {
+          if (k < total) {
+            if (starts(info[0]) && !stage_q(seg_of(info[0]))) break;
+            const uint4 *krow = row_ptr(kc, slot[0], head_of(info[0]), kDqk);
+            const int s = k & 1;
+            load(buf, 12, krow, slot[0]);
+            if (k >= 2 && !tc::mbar_wait_warp(&bars.k_empty[s], ((k >> 1) - 1) & 1, &abort_flag)) break;
+            const uint32_t kb = sbase + kOffK + s * kKStage;
+  #pragma unroll
+            for (int i = 0; i < 12; ++i) put(kb, i, buf[i]);
+            load(buf, 12, krow + 12, slot[0]);
+  #pragma unroll
+            for (int i = 0; i < 12; ++i) put(kb, 12 + i, buf[i]);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive_warp(&bars.k_full[s]);
+          }
+          if (k >= 1) {
+            const uint4 *vrow = row_ptr(vc, v_slot, v_g, kDv);
+            load(buf, 8, vrow, v_slot);
+            if (k >= 2 && !tc::mbar_wait_warp(&bars.v_empty, (k - 2) & 1, &abort_flag)) break;
+  #pragma unroll
+            for (int i = 0; i < 8; ++i) put(sbase + kOffV, i, buf[i]);
+            load(buf, 8, vrow + 8, v_slot);
+  #pragma unroll
+            for (int i = 0; i < 8; ++i) put(sbase + kOffV, 8 + i, buf[i]);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive_warp(&bars.v_full);
+          }
+          if (k < total) {
+            v_slot = slot[0];
+            v_g = head_of(info[0]);
+            shift(k);
+          }
+        }
+      }
+      if (bad_page) atomicOr(a.err, 1);
     }
-    if (bad_page) atomicOr(a.err, 1);
   } else if (warp >= kMmaWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
     if (warp > kMmaWarp + 1) goto done;   // warps 14-15: idle
@@ -826,21 +891,29 @@ done:
 
 }  // namespace
 
-cudaError_t launch_attn_prefill(const HostPlan &hp, const RunArgs &a, cudaStream_t stream) {
+cudaError_t launch_attn_prefill(const HostPlan &hp, const RunArgs &a, const TmaMaps *stage,
+                                cudaStream_t stream) {
   if (hp.num_ctas == 0) return cudaSuccess;
-  if (hp.prob.kv_dtype == ATTN_KV_FP8_E4M3)
-    return launch_dependent(attn_prefill_kernel<true>, dim3(hp.num_ctas), dim3(kPThreads), kSmem,
-                            stream, a);
-  return launch_dependent(attn_prefill_kernel<false>, dim3(hp.num_ctas), dim3(kPThreads), kSmem,
-                          stream, a);
+  const dim3 grid(hp.num_ctas), block(kPThreads);
+  const TmaMaps none{};
+  const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
+  if (stage)
+    return fp8 ? launch_dependent(attn_prefill_kernel<true, true>, grid, block, kSmem, stream, a, *stage)
+               : launch_dependent(attn_prefill_kernel<false, true>, grid, block, kSmem, stream, a,
+                                  *stage);
+  return fp8 ? launch_dependent(attn_prefill_kernel<true, false>, grid, block, kSmem, stream, a, none)
+             : launch_dependent(attn_prefill_kernel<false, false>, grid, block, kSmem, stream, a,
+                                none);
 }
 
 cudaError_t prepare_attn_prefill(const HostPlan &hp) {
-  return hp.prob.kv_dtype == ATTN_KV_FP8_E4M3
-             ? cudaFuncSetAttribute(attn_prefill_kernel<true>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)
-             : cudaFuncSetAttribute(attn_prefill_kernel<false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  const bool fp8 = hp.prob.kv_dtype == ATTN_KV_FP8_E4M3;
+  cudaError_t e = cudaFuncSetAttribute(fp8 ? attn_prefill_kernel<true, true> : attn_prefill_kernel<false, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fp8 ? attn_prefill_kernel<true, false> : attn_prefill_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  return e;
 }
 
 }  // namespace akp

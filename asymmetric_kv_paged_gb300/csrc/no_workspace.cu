@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "attn_paged.h"
+#include "kernels.hpp"
 #include "plan.hpp"
 
 namespace {
@@ -55,14 +56,16 @@ extern "C" attn_status_t attn_run_paged_no_workspace(
     const float *sinks, int32_t window, float softmax_scale, float k_scale, float v_scale,
     void *out, float *lse_out, void *stream) {
   if (!plan || plan->device < 0) return ATTN_ERR_INVALID_ARG;
-  if (plan->host.workspace_bytes > (size_t)ATTN_NO_WORKSPACE_MAX_BYTES) return ATTN_ERR_WORKSPACE;
+  // the split partials must fit; a prefill plan's K/V staging scratch is not
+  // used here (its prefill kernel then reads the paged caches itself)
+  if (plan->host.partial_bytes > (size_t)ATTN_NO_WORKSPACE_MAX_BYTES) return ATTN_ERR_WORKSPACE;
   void *scratch = nullptr;
   const attn_status_t st = scratch_address(plan->device, &scratch);
   if (st != ATTN_OK) return st;
   // Nothing in the scratch has to start at zero: every partial the merge reads
   // is written earlier in the same call, so the previous call's leftovers are
   // never used.
-  return attn_run_paged(plan, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks, window,
-                        softmax_scale, k_scale, v_scale, out, lse_out, scratch,
-                        (size_t)ATTN_NO_WORKSPACE_MAX_BYTES, stream);
+  return akp::run_paged_unstaged(plan, q, k_cache, v_cache, page_table, seq_lens, qo_indptr, sinks,
+                                 window, softmax_scale, k_scale, v_scale, out, lse_out, scratch,
+                                 (size_t)ATTN_NO_WORKSPACE_MAX_BYTES, stream);
 }

@@ -22,11 +22,12 @@ constexpr int kPrefillKeyTile = 128;   // keys per tile of the prefill kernel
 // 128, else 256: the prefill kernel's two 128-row Q tiles over 128-key tiles.
 
 // One row block: rows [row0, row0 + nrows) of (b, g).  Keys [klo, khi) are
-// the union of what its rows can see.
+// the union of what its rows can see.  srow: with a staging scratch (prefill
+// plans, see StageUnit), key j of (b, g) is scratch row srow + j; else 0.
 struct BlockDesc {
   int32_t b, g, row0, nrows;
   int32_t L, n, tok0, klo;        // seq len, new tokens, first flat token, first key
-  int32_t khi, num_splits, part_row_base, pad0;
+  int32_t khi, num_splits, part_row_base, srow;
 };
 static_assert(sizeof(BlockDesc) == 48, "BlockDesc layout");
 
@@ -45,6 +46,19 @@ struct CtaHead {
   BlockDesc blk;
 };
 static_assert(sizeof(CtaHead) == 80, "CtaHead layout");
+
+// Prefill plans stage the keys their blocks read into a scratch of 16-bit
+// rows (E4M3 widened to fp16, BF16 copied) once per call, which the prefill
+// kernel then loads as whole tiles by TMA.  One unit per (request, KV head)
+// with prefill blocks: keys [j0, j0 + 128 * tiles) go to scratch rows
+// [row_base, ...); keys outside [klo, khi) (the union of the unit's blocks'
+// ranges) are written as zeros.  tile_off: the unit's first tile among all
+// units' tiles.
+struct StageUnit {
+  int32_t b, g, j0, klo, khi, tiles, row_base, tile_off;
+};
+static_assert(sizeof(StageUnit) == 32, "StageUnit layout");
+constexpr int kStageTile = 128;      // keys per staged tile (the prefill key tile)
 
 // One merge item: rows [row_begin, row_begin + 8) of a multi-split block.
 struct MergeItem {
@@ -68,7 +82,12 @@ struct HostPlan {
   std::vector<CtaHead> cta_heads;      // [num_ctas]
   std::vector<MergeItem> merge_items;
   int64_t part_rows = 0;
-  size_t workspace_bytes = 0;
+  // staging scratch (prefill plans that are not replayable; empty otherwise)
+  std::vector<StageUnit> stage_units;
+  int64_t stage_rows = 0, stage_tiles = 0;
+  size_t partial_bytes = 0;      // split partials: part_o then part_lse
+  size_t stage_bytes = 0;        // staged K rows then staged V rows, after the partials
+  size_t workspace_bytes = 0;    // partial_bytes + stage_bytes
   int32_t multi_split_blocks = 0;
   bool use_tma = false;          // K/V tiles as TMA boxes (else gathered by threads)
   // Replayable plans: seq_lens holds the per-request upper bounds, the work
@@ -85,6 +104,7 @@ struct DevicePlan {
   int32_t *cta_seg_begin = nullptr;
   CtaHead *cta_heads = nullptr;
   MergeItem *merge_items = nullptr;
+  StageUnit *stage_units = nullptr;
   int32_t *err = nullptr;  // device error word
   // replayable plans only
   int32_t *seq_bounds = nullptr;   // [B]
@@ -112,6 +132,13 @@ inline size_t part_o_bytes(int64_t part_rows) {
 }
 inline size_t part_lse_bytes(int64_t part_rows) {
   return ((size_t)part_rows * sizeof(float) + 255) & ~(size_t)255;
+}
+// Staging scratch: K rows (dqk 16-bit values each), then V rows (kDv each).
+inline size_t stage_k_bytes(int64_t rows, int dqk) {
+  return ((size_t)rows * dqk * 2 + 255) & ~(size_t)255;
+}
+inline size_t stage_v_bytes(int64_t rows) {
+  return ((size_t)rows * kDv * 2 + 255) & ~(size_t)255;
 }
 
 }  // namespace akp

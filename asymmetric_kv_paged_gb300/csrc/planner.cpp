@@ -25,6 +25,60 @@ void fill_cta_heads(HostPlan *hp) {
     hp->cta_heads[c] = cta_head(hp->segs.data(), hp->blocks.data(), hp->cta_seg_begin[c],
                                 hp->cta_seg_begin[c + 1]);
 }
+
+// Staging units of a prefill plan: one per (request, KV head), over the
+// 128-key tiles that hold the union of its blocks' key ranges (blocks come in
+// (b, g, row0) order, so a unit's blocks are consecutive).  Each block learns
+// where its keys sit in the scratch (srow).  Without a prefill plan, or if
+// the scratch rows would overflow the int32 coordinates of a TMA copy, there
+// is no scratch and the prefill kernel reads the cache itself.
+void build_stage(HostPlan *hp) {
+  hp->stage_units.clear();
+  hp->stage_rows = hp->stage_tiles = 0;
+  for (BlockDesc &bd : hp->blocks) bd.srow = 0;
+  if (!hp->prefill || hp->replayable) return;
+  const int64_t nb = (int64_t)hp->blocks.size();
+  for (int64_t first = 0; first < nb;) {
+    const BlockDesc &b0 = hp->blocks[first];
+    int64_t end = first;
+    int32_t klo = b0.klo, khi = b0.khi;
+    while (end < nb && hp->blocks[end].b == b0.b && hp->blocks[end].g == b0.g) {
+      klo = std::min(klo, hp->blocks[end].klo);
+      khi = std::max(khi, hp->blocks[end].khi);
+      ++end;
+    }
+    StageUnit u{};
+    u.b = b0.b;
+    u.g = b0.g;
+    u.j0 = klo / kStageTile * kStageTile;
+    u.klo = klo;
+    u.khi = khi;
+    u.tiles = (khi - 1) / kStageTile - klo / kStageTile + 1;
+    if (hp->stage_rows + (int64_t)u.tiles * kStageTile > INT32_MAX - kStageTile) {
+      hp->stage_units.clear();
+      hp->stage_rows = hp->stage_tiles = 0;
+      for (BlockDesc &bd : hp->blocks) bd.srow = 0;
+      return;
+    }
+    u.row_base = (int32_t)hp->stage_rows;
+    u.tile_off = (int32_t)hp->stage_tiles;
+    for (int64_t bi = first; bi < end; ++bi) hp->blocks[bi].srow = u.row_base - u.j0;
+    hp->stage_rows += (int64_t)u.tiles * kStageTile;
+    hp->stage_tiles += u.tiles;
+    hp->stage_units.push_back(u);
+    first = end;
+  }
+}
+
+// Workspace: split partials, then (prefill plans) the staging scratch.
+void size_workspace(HostPlan *hp) {
+  hp->partial_bytes =
+      hp->part_rows ? part_o_bytes(hp->part_rows) + part_lse_bytes(hp->part_rows) : 0;
+  hp->stage_bytes = hp->stage_rows ? stage_k_bytes(hp->stage_rows, hp->prob.head_dim_qk) +
+                                         stage_v_bytes(hp->stage_rows)
+                                   : 0;
+  hp->workspace_bytes = hp->partial_bytes + hp->stage_bytes;
+}
 }  // namespace
 
 
@@ -196,7 +250,8 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
     }
   }
   if (hp.part_rows > INT32_MAX / kDv) return ATTN_ERR_UNSUPPORTED;
-  hp.workspace_bytes = hp.part_rows ? part_o_bytes(hp.part_rows) + part_lse_bytes(hp.part_rows) : 0;
+  build_stage(&hp);
+  size_workspace(&hp);
   fill_cta_heads(&hp);
   *out = std::move(hp);
   return ATTN_OK;
@@ -225,7 +280,8 @@ attn_status_t build_replayable_plan(const attn_problem_t *p, int32_t num_sms, Ho
   // most nb + num_ctas - 1 segments in all
   hp.part_rows = (int64_t)max_rows * hp.seg_capacity;
   if (hp.part_rows > INT32_MAX / kDv) return ATTN_ERR_UNSUPPORTED;
-  hp.workspace_bytes = hp.part_rows ? part_o_bytes(hp.part_rows) + part_lse_bytes(hp.part_rows) : 0;
+  build_stage(&hp);     // no scratch: the work list changes from run to run
+  size_workspace(&hp);
   // merge items for every block: the merge skips blocks a run leaves whole
   hp.merge_items.clear();
   for (int64_t bi = 0; bi < nb; ++bi)

@@ -389,6 +389,28 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// ---------------------------------------------------------------- TMA
+
+// One arrival on `bar` that also expects `bytes` of asynchronous copies.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Tiled TMA load of the box at (x, y) of a 2D tensor map (`map` points to a
+// __grid_constant__ parameter) into shared memory at `dst`, completing as
+// transaction bytes on `bar`.  x times the element size must be a multiple of
+// 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Byte offset of element (row, col) of a 16-bit tile stored as 128-byte
 // swizzled rows (64 elements per row, 8-row / 1024-byte atoms): the 16-byte
 // chunk index is XORed with row % 8, matching the 128B swizzle mode.

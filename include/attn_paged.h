@@ -178,7 +178,13 @@ attn_status_t attn_plan_replayable(const attn_problem_t *bounds, int device, att
  * 2^-31 of that maximum stays exact in fp16), E4M3 is widened exactly to
  * fp16, and the scores are divided by the same power of two in fp32; P.V
  * is fp16 x fp16 with fp32 accumulation.  The E4M3 NaN codes (0x7F, 0xFF) in
- * a visible slot are not propagated (they read as +-480).
+ * a visible slot read as +-480 on the decode/verify plans and stay NaN on the
+ * prefill plans.
+ * Prefill plans that are not replayable first gather the keys their blocks
+ * read into a staging scratch in the workspace (16-bit rows: E4M3 widened
+ * exactly to fp16, BF16 copied; (Dqk + 128) * 2 bytes per key of each KV
+ * head, over whole 128-key tiles), which the prefill kernel loads as TMA
+ * tiles; attn_plan's workspace size includes it.
  * Runs of one plan must be ordered on one stream (they share the plan's
  * device error word); different plans are independent.
  * Errors: INVALID_ARG, WORKSPACE, CUDA (launch errors; nothing is waited for).
@@ -258,8 +264,10 @@ attn_status_t attn_append_kv(attn_plan_t plan, const void *k_new, const void *v_
  *     device (a host-side query, no allocation); make that first call before
  *     any stream capture.  The address is kept for the life of the process
  *     and is stale after cudaDeviceReset (as are plans made before it).
- *   - Plans whose workspace_bytes exceed ATTN_NO_WORKSPACE_MAX_BYTES are
- *     rejected with ATTN_ERR_WORKSPACE before anything is launched.
+ *   - Plans whose split partials exceed ATTN_NO_WORKSPACE_MAX_BYTES are
+ *     rejected with ATTN_ERR_WORKSPACE before anything is launched.  A
+ *     prefill plan's K/V staging scratch is not used: its prefill kernel
+ *     reads the paged caches itself (same results).
  *   - All calls share the one array, and it keeps whatever the last call left
  *     in it; nothing in it needs to start at zero, because each call writes
  *     every partial it later reads.  Calls whose kernels overlap on the GPU
@@ -327,10 +335,23 @@ attn_status_t attn_plan_segments(attn_plan_t plan, int32_t *segments_host);
  *   {seg_begin, seg_end, key tiles in all its segments, 0,
  *    its first segment {block, tile_begin, tile_end, split},
  *    that segment's block {b, g, row0, nrows, L, n, tok0, key_lo, key_hi,
- *    num_splits, part_row_base, 0}}
- * (zeros after the range for a CTA without segments).  Errors: INVALID_ARG.
+ *    num_splits, part_row_base, srow}}
+ * (zeros after the range for a CTA without segments), where srow places the
+ * block's keys in the staging scratch (key j of its (b, g) is scratch row
+ * srow + j; 0 for plans without one).  Errors: INVALID_ARG.
  */
 attn_status_t attn_plan_cta_heads(attn_plan_t plan, int32_t *heads_host);
+/*
+ * attn_plan_stage_units reports a prefill plan's staging units, one per
+ * (request, KV head) with prefill blocks: *count units (0 for plans without a
+ * staging scratch) and, when units_host is not NULL, 8 int32 per unit:
+ *   {b, g, j0, key_lo, key_hi, tiles, row_base, tile_off}
+ * Keys [j0, j0 + 128 * tiles) (j0 a multiple of 128) occupy scratch rows
+ * [row_base, row_base + 128 * tiles); keys outside [key_lo, key_hi), the
+ * union of the unit's blocks' key ranges, are staged as zeros; tile_off is
+ * the unit's first tile among all units'.  Errors: INVALID_ARG.
+ */
+attn_status_t attn_plan_stage_units(attn_plan_t plan, int32_t *count, int32_t *units_host);
 attn_status_t attn_plan_replayable_host(const attn_problem_t *bounds, int32_t num_sms,
                                         attn_plan_t *plan);
 attn_status_t attn_plan_replan_host(attn_plan_t plan, const int32_t *seq_lens_host,

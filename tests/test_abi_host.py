@@ -135,10 +135,11 @@ def _coverage_check(w, num_sms):
     return _check_plan(B.attn_plan_host(prob, num_sms, keep), w, num_sms)
 
 
-def _check_plan(plan, w, num_sms):
+def _check_plan(plan, w, num_sms, replayable=False):
     """The plan's work list covers every (request, KV head, row) once, with the
     key range its rows see, each block's tiles once in split order, and CTA
-    loads balanced; returns the plan's info."""
+    loads balanced; a static prefill plan stages each (request, KV head)'s keys
+    once; returns the plan's info."""
     info = B.attn_plan_info(plan)
     blocks = B.attn_plan_blocks(plan)
     segs = B.attn_plan_segments(plan)
@@ -193,6 +194,37 @@ def _check_plan(plan, w, num_sms):
         assert list(h[4:8]) == list(segs[mine[0], 1:5])
         bi = segs[mine[0], 1]
         assert list(h[8:12]) == list(blocks[bi, :4]) and list(h[15:19]) == list(blocks[bi, 4:8])
+    # Staging units (static prefill plans only): one per (request, KV head)
+    # with blocks, over whole 128-key tiles from the tile of the smallest key_lo
+    # to that of the largest key_hi, rows and tiles laid out back to back in
+    # unit order; a block's head record places its keys at row srow + j.
+    units = B.attn_plan_stage_units(plan)
+    if R != 256 or replayable:
+        assert len(units) == 0
+        assert all(heads[c][19] == 0 for c in range(info["ctas"]))
+        return info
+    expect_units = {}
+    for (b, g, row0, nrows, klo, khi, nsplit, prb) in blocks:
+        lo, hi = expect_units.get((b, g), (klo, khi))
+        expect_units[(b, g)] = (min(lo, klo), max(hi, khi))
+    assert len(units) == len(expect_units)
+    row = tiles = 0
+    srow = {}
+    for (b, g, j0, klo, khi, ntiles, row_base, tile_off) in units:
+        assert expect_units[(b, g)] == (klo, khi)
+        assert j0 == klo // 128 * 128 and j0 + 128 * ntiles >= khi > j0 + 128 * (ntiles - 1)
+        assert row_base == row and tile_off == tiles
+        row += 128 * ntiles
+        tiles += ntiles
+        srow[(b, g)] = row_base - j0
+    align = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    part = int(blocks[:, 6][blocks[:, 6] > 1].dot(blocks[:, 3][blocks[:, 6] > 1]))
+    partial = align(part * 128 * 4) + align(part * 4) if part else 0
+    assert info["workspace_bytes"] == partial + align(row * w.dqk * 2) + align(row * 128 * 2)
+    for c in range(info["ctas"]):
+        if heads[c][1] > heads[c][0]:
+            b, g = heads[c][8], heads[c][9]
+            assert heads[c][19] == srow[(b, g)]
     return info
 
 
@@ -203,6 +235,7 @@ def _check_plan(plan, w, num_sms):
     dict(seq=[190, 333], n=[5, 1], hq=2, hkv=2, P=1, W=4),
     dict(seq=[3000], n=[300], hq=64, hkv=4, P=128, W=0),
     dict(seq=[1000, 1000, 1000], n=[1, 8, 1], hq=16, hkv=2, P=128, W=128),
+    dict(seq=[5000, 700, 260], n=[40, 1, 20], hq=16, hkv=2, P=16, W=300),   # windowed prefill
 ])
 @pytest.mark.parametrize("num_sms", [1, 7, 152])
 def test_schedule_covers_every_key_once(case, num_sms):
@@ -346,7 +379,7 @@ def test_replayable_replan_keeps_schedule_invariants(seed):
         elif trial == 1:
             lens = n.copy()                              # only the new tokens
         assert B.attn_plan_replan_host(plan, lens) == 0
-        info = _check_plan(plan, _with_lens(w, lens), num_sms)
+        info = _check_plan(plan, _with_lens(w, lens), num_sms, replayable=True)
         assert info["ctas"] == info0["ctas"] and info["blocks"] == info0["blocks"]
         assert info["segments"] <= info["blocks"] + info["ctas"]
         segs = B.attn_plan_segments(plan)

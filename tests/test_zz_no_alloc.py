@@ -55,6 +55,42 @@ def test_no_workspace_matches_workspace_path_twice():
     assert B.attn_get_device_error(dw.plan) == 0
 
 
+@pytest.mark.parametrize("case", [
+    # name, seq_lens, new tokens, hq, hkv, page size, window, sinks, kv dtype
+    ("fp8_p128", [1500, 700], [40, 1], 16, 2, 128, 0, False, "fp8"),
+    ("bf16_p16_window_sinks", [2600, 90], [200, 40], 16, 2, 16, 300, True, "bf16"),
+    ("fp8_p1_window", [1500], [160], 8, 1, 1, 700, False, "fp8"),
+])
+def test_prefill_staged_equals_direct_cache_reads(case):
+    """A prefill plan run with a workspace stages its keys into 16-bit scratch
+    rows that the prefill kernel loads by TMA; without one (this entry point)
+    the prefill kernel reads the paged caches itself.  The operand tiles hold
+    the same values for every key a row can see, and keys it cannot see are
+    masked to exact zeros of P either way, so the two give the same output."""
+    from asymmetric_kv_paged_gb300 import binding as B
+    from asymmetric_kv_paged_gb300.runner import DeviceWorkload
+    name, seq, n, hq, hkv, P, win, sinks, kv = case
+    w = W.make_workload(77, seq, n, hq=hq, hkv=hkv, page_size=P, window=win, sinks=sinks,
+                        kv_dtype=kv, name=name)
+    dw = DeviceWorkload(w)
+    info = B.attn_plan_info(dw.plan)
+    assert info["rows_per_block"] == 256 and len(B.attn_plan_stage_units(dw.plan)) > 0
+    dw.run()
+    torch.cuda.synchronize()
+    assert B.attn_get_device_error(dw.plan) == 0
+    ref = dw.out.float().clone()
+    ref_lse = dw.lse.clone()
+    out = torch.full_like(dw.out, float("nan"))
+    lse = torch.full_like(dw.lse, float("nan"))
+    B.attn_run_paged_no_workspace(dw.plan, dw.q, dw.k_cache, dw.v_cache, dw.page_table,
+                                  dw.seq_lens, dw.qo_indptr, dw.sinks, w.window,
+                                  w.softmax_scale, w.k_scale, w.v_scale, out, lse)
+    torch.cuda.synchronize()
+    assert B.attn_get_device_error(dw.plan) == 0
+    assert torch.isfinite(out.float()).all()
+    assert torch.equal(out.float(), ref) and torch.equal(lse, ref_lse)
+
+
 def test_no_workspace_rejects_plans_above_the_limit():
     from asymmetric_kv_paged_gb300 import binding as B
     t = torch.zeros(16, dtype=torch.int32, device="cuda")
