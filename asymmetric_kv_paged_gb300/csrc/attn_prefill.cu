@@ -12,13 +12,16 @@
 // and MMA warpgroups to the softmax ones after the start):
 //   warps 0-3   softmax + epilogue of Q tile 0 (row p in TMEM lane p);
 //   warps 4-7   the same for Q tile 1;
-//   warps 8-11  load warps: per key tile, the page lookup of each key, K and V
-//               rows read from the cache with 16-byte loads (one thread per
-//               key), E4M3 widened exactly to fp16 in registers (the MMAs of
-//               an FP8 cache run in fp16), and the rows stored into the
-//               128-byte-swizzled operand tiles; the Q rows of each new block
-//               (for FP8 caches scaled per row by a power of two, see
-//               q_row_shift);
+//   warps 8-11  load warps: the Q rows of each new block (for FP8 caches
+//               scaled per row by a power of two, see q_row_shift), and the
+//               K/V tiles.  With a staging scratch (kv_stage.cu: every key of
+//               the block's (request, KV head) already a 16-bit row, E4M3
+//               widened exactly to fp16) one thread issues each tile as TMA
+//               boxes in the operand layout.  Without one, per key tile: the
+//               page lookup of each key, K and V rows read from the cache with
+//               16-byte loads (one thread per key), widened in registers, and
+//               stored into the 128-byte-swizzled operand tiles.  (The MMAs of
+//               an FP8 cache run in fp16.)
 //   warp  12    TMEM allocation; one thread issues the MMAs of Q tile 0;
 //   warp  13    one thread issues the MMAs of Q tile 1;
 //   warps 14-15 idle (they complete the fourth warpgroup).
@@ -568,8 +571,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
       cm.init(a.segs, a.blocks, head);
       int ct = 0;      // key tiles with rows in this Q tile
       int segs_t = 0;  // finished segments with rows in this Q tile
-      int n1 = 0;      // (thread 0) key tiles so far that had Q tile 1 rows
-      bool prev1 = false;
       for (int k = 0; k < total; ++k, cm.next()) {
         const bool has1 = cm.bd.nrows > kPM;
         const bool mine = t == 0 || has1;
@@ -581,15 +582,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
           // S_t of this tile overwrites P_t of the previous one, which P_t.V
           // reads: that MMA was issued before these by this same thread, and
           // the tensor pipe runs one thread's MMAs in issue order, so there
-          // is nothing to wait for.
-          // The two Q tiles take turns: S1 of a tile is issued once S0 of it is
-          // done, S0 once S1 of the previous tile is.  Their softmaxes then run
-          // half a tile apart, each while the tensor pipe works for the other,
-          // instead of both at once with the pipe idle.  (Neither barrier can
-          // run two phases ahead of this wait: each phase needs the other.)
-          if (t == 1 && !tc::mbar_wait_spin(&bars.s_full[0], k & 1, &abort_flag)) break;
-          if (t == 0 && prev1 && !tc::mbar_wait_spin(&bars.s_full[1], (n1 - 1) & 1, &abort_flag))
-            break;
+          // is nothing to wait for.  The two Q tiles' chains are not paced
+          // against each other: each thread issues as soon as its own inputs
+          // are ready (making S1 of a tile wait for S0 of it, and S0 for S1 of
+          // the previous tile, measured 4% slower once K/V came by TMA).
           tc::tc_fence_after();
 #pragma unroll
           for (int kq = 0; kq < kDqk / 16; ++kq) {
@@ -625,8 +621,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (cm.last()) ++segs_t;
         }
         tc::mma_commit(&bars.v_empty);
-        n1 += has1;
-        prev1 = has1;
       }
       // every MMA issued must be complete before TMEM is released, also
       // after a give-up (a wait of its own, bounded, that ignores the abort)
