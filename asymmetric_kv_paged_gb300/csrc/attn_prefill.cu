@@ -558,8 +558,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // finish, the other keeps the tensor pipe fed.  The K, V and Q stages go
     // back to the load warps once both threads have committed (count 2); the
     // thread of Q tile 1 commits on tiles without Q tile 1 rows too.  The
-    // threads poll their barriers: one woken from a suspended wait resumes
-    // hundreds of cycles after the phase completes.
+    // threads sleep on their barriers (mbarrier try_wait) rather than poll
+    // them: a polling thread takes issue slots from the softmax warps of its
+    // SM sub-partition, whose P it is waiting for (polling measured 2.5%
+    // slower on the chunked prefill).
     if ((tid & 31) == 0) {
       const int t = warp - kMmaWarp;
       const uint32_t id_s = tc::idesc_f16(FP8 ? 0 : 1, 0, 0, kPM, kPN);     // fp16 for FP8 caches
@@ -576,8 +578,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const bool mine = t == 0 || has1;
         const bool first = cm.first();
         const int s = k & 1;
-        if (first && !tc::mbar_wait_spin(&bars.q_full, cm.si & 1, &abort_flag)) break;
-        if (!tc::mbar_wait_spin(&bars.k_full[s], (k >> 1) & 1, &abort_flag)) break;
+        if (first && !tc::mbar_wait(&bars.q_full, cm.si & 1, &abort_flag)) break;
+        if (!tc::mbar_wait(&bars.k_full[s], (k >> 1) & 1, &abort_flag)) break;
         if (mine) {
           // S_t of this tile overwrites P_t of the previous one, which P_t.V
           // reads: that MMA was issued before these by this same thread, and
@@ -598,11 +600,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         tc::mma_commit(&bars.k_empty[s]);
         if (cm.last()) tc::mma_commit(&bars.q_empty);
-        if (!tc::mbar_wait_spin(&bars.v_full, k & 1, &abort_flag)) break;
+        if (!tc::mbar_wait(&bars.v_full, k & 1, &abort_flag)) break;
         if (mine) {
-          if (!tc::mbar_wait_spin(&bars.p_hi[t], ct & 1, &abort_flag)) break;
+          if (!tc::mbar_wait(&bars.p_hi[t], ct & 1, &abort_flag)) break;
           // the first P.V of a segment overwrites O: the previous epilogue must have read it
-          if (first && segs_t > 0 && !tc::mbar_wait_spin(&bars.o_free[t], (segs_t - 1) & 1, &abort_flag))
+          if (first && segs_t > 0 && !tc::mbar_wait(&bars.o_free[t], (segs_t - 1) & 1, &abort_flag))
             break;
           // keys 64-127 first (their P is ready first), then keys 0-63
           auto pv = [&](int kk, bool acc) {
@@ -612,7 +614,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tc::tc_fence_after();
 #pragma unroll
           for (int kk = kPN / 32; kk < kPN / 16; ++kk) pv(kk, !first || kk > kPN / 32);
-          if (!tc::mbar_wait_spin(&bars.p_full[t], ct & 1, &abort_flag)) break;
+          if (!tc::mbar_wait(&bars.p_full[t], ct & 1, &abort_flag)) break;
           tc::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kPN / 32; ++kk) pv(kk, true);
