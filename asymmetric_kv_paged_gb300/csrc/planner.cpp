@@ -173,8 +173,8 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   // Deal tiles to CTAs in block order, cutting a block where a CTA's share
   // ends.  Each new CTA's share is the remaining tiles over the remaining
   // CTAs, so rounding never piles up on the last one; a block remainder of at
-  // most `slack` tiles (1/32 of a share) stays on the current CTA rather than
-  // becoming a split of its own.
+  // most `slack` tiles (1/32 of a share; two for prefill plans) stays on the
+  // current CTA rather than becoming a split of its own.
   const int64_t nb = (int64_t)hp.blocks.size();
   constexpr int64_t kWholeBlockTiles = 8;
   // A CTA that goes on to a further segment pays for the switch (the finished
@@ -204,7 +204,10 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
           charge = cta + 1 < num_sms && target >= 8 * kSegSwitchTiles;
           if (charge)
             target = (remaining + kSegSwitchTiles * (nb - bi - 1) + ctas_left - 1) / ctas_left;
-          slack = target / 32;
+          // A prefill tile (128 keys x 256 rows) costs far more than the
+          // split it would save: there the slack is at most two tiles
+          // (measured: 1/32 of a share left CTAs 2.5% apart in tiles and time).
+          slack = hp.prefill ? std::min<int64_t>(2, target / 32) : target / 32;
           room = target;
         }
         const int64_t left = tend - t0;
