@@ -23,6 +23,7 @@ ATTN_KV_FP8_E4M3 = 1
 EXPORTED = ("attn_plan", "attn_run_paged", "attn_run_phase", "attn_plan_destroy", "attn_get_device_error",
             "attn_status_string", "attn_plan_host", "attn_plan_info", "attn_plan_blocks",
             "attn_plan_segments", "attn_plan_cta_heads", "attn_plan_stage_units",
+            "attn_plan_merge_ctas",
             "attn_debug_tc_gemm",
             "attn_run_paged_no_workspace",
             "attn_append_kv", "attn_plan_replayable", "attn_plan_replayable_host",
@@ -299,6 +300,14 @@ def attn_plan_cta_heads(plan: Plan):
                                       arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
            "attn_plan_cta_heads")
     return arr[:n]
+
+
+def attn_plan_merge_ctas(plan: Plan) -> int:
+    """CTAs of the merge kernel a run of `plan` launches (0: none)."""
+    n = ctypes.c_int32(0)
+    _check(load().attn_plan_merge_ctas(ctypes.c_void_p(plan.handle), ctypes.byref(n)),
+           "attn_plan_merge_ctas")
+    return n.value
 
 
 def attn_plan_stage_units(plan: Plan):

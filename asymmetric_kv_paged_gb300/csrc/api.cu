@@ -484,6 +484,12 @@ attn_status_t attn_plan_cta_heads(attn_plan_t plan, int32_t *heads_host) {
   return ATTN_OK;
 }
 
+attn_status_t attn_plan_merge_ctas(attn_plan_t plan, int32_t *ctas) {
+  if (!plan || !ctas) return ATTN_ERR_INVALID_ARG;
+  *ctas = (int32_t)plan->host.merge_items.size();
+  return ATTN_OK;
+}
+
 attn_status_t attn_plan_stage_units(attn_plan_t plan, int32_t *count, int32_t *units_host) {
   if (!plan || !count) return ATTN_ERR_INVALID_ARG;
   const std::vector<akp::StageUnit> &u = plan->host.stage_units;

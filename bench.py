@@ -238,7 +238,13 @@ def time_workload(dw, steps: int, warmup: int, world: int, flush_l2: bool = Fals
     for _ in range(warmup):
         dw.run_phase(0, stream)
         dw.run_phase(1, stream)
-    has_merge = dw.plan.workspace_bytes > 0
+    from asymmetric_kv_paged_gb300 import binding
+    # kernels per step: the attention kernel, the merge kernel when the plan
+    # leaves blocks to it, the staging pass of a prefill plan, the device
+    # planner of a replayable plan
+    per_step = (1 + (binding.attn_plan_merge_ctas(dw.plan) > 0)
+                + (len(binding.attn_plan_stage_units(dw.plan)) > 0)
+                + bool(getattr(dw, "replayable", False)))
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -280,7 +286,7 @@ def time_workload(dw, steps: int, warmup: int, world: int, flush_l2: bool = Fals
     step = float(np.mean([e[0].elapsed_time(e[1]) for e in ev2]))
     total = start.elapsed_time(end) / steps
     return dict(step_ms=(step if flush_l2 else total), split_ms=split, merge_ms=merge,
-                attn_ms=step, t0=t0, t1=t1, launches=steps * (2 if has_merge else 1))
+                attn_ms=step, t0=t0, t1=t1, launches=steps * per_step)
 
 
 def grown_workload(w, extra: int):

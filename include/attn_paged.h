@@ -352,6 +352,13 @@ attn_status_t attn_plan_cta_heads(attn_plan_t plan, int32_t *heads_host);
  * the unit's first tile among all units'.  Errors: INVALID_ARG.
  */
 attn_status_t attn_plan_stage_units(attn_plan_t plan, int32_t *count, int32_t *units_host);
+/*
+ * attn_plan_merge_ctas reports in *ctas how many CTAs the merge kernel of a
+ * run launches (0: the run launches no merge kernel): one per 8 rows of every
+ * multi-split block (of every block for a replayable plan, whose splits are
+ * only known on the device).  Errors: INVALID_ARG.
+ */
+attn_status_t attn_plan_merge_ctas(attn_plan_t plan, int32_t *ctas);
 attn_status_t attn_plan_replayable_host(const attn_problem_t *bounds, int32_t num_sms,
                                         attn_plan_t *plan);
 attn_status_t attn_plan_replan_host(attn_plan_t plan, const int32_t *seq_lens_host,
