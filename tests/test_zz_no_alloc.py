@@ -55,6 +55,39 @@ def test_no_workspace_matches_workspace_path_twice():
     assert B.attn_get_device_error(dw.plan) == 0
 
 
+def test_no_workspace_under_graph_capture():
+    """The entry point is meant for callers that capture the step in a CUDA
+    graph: after one eager call (which looks the scratch address up), a
+    captured call replays with the workspace path's bits and no device error."""
+    from asymmetric_kv_paged_gb300 import binding as B
+    w, dw = _device_workload()
+    dw.run()
+    torch.cuda.synchronize()
+    ref = dw.out.float().clone()
+    ref_lse = dw.lse.clone()
+    out = torch.empty_like(dw.out)
+    lse = torch.empty_like(dw.lse)
+
+    def call(stream):
+        B.attn_run_paged_no_workspace(dw.plan, dw.q, dw.k_cache, dw.v_cache, dw.page_table,
+                                      dw.seq_lens, dw.qo_indptr, dw.sinks, w.window,
+                                      w.softmax_scale, w.k_scale, w.v_scale, out, lse, stream)
+
+    call(torch.cuda.current_stream())          # eager first: the scratch address lookup
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(s)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.float(), ref) and torch.equal(lse, ref_lse)
+    assert B.attn_get_device_error(dw.plan) == 0
+
+
 @pytest.mark.parametrize("case", [
     # name, seq_lens, new tokens, hq, hkv, page size, window, sinks, kv dtype
     ("fp8_p128", [1500, 700], [40, 1], 16, 2, 128, 0, False, "fp8"),
