@@ -245,12 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (seg_begin >= seg_end) return;
   const int total = head.total;
   if constexpr (HALF) {
-    // Verify plans: the producer warp warms the page-table entries of the
-    // CTA's first four tiles (an L2 prefetch, clamped to the block's entries)
-    // while the barriers are set up, so that the first TMA issue does not
-    // wait on a DRAM round trip (c3a 59.8 -> 57.4 us with L2 flushed; the
-    // same prefetch in the decode instantiation measured 1 us slower on the
-    // batched decode).
+    // Verify plans: while the barriers are set up, the producer warp warms
+    // the page-table entries of the CTA's first four tiles and the converter
+    // warps the first block's Q rows (L2 prefetches, within the block's own
+    // entries and rows), so that neither the first TMA issue nor the first Q
+    // staging waits on a DRAM round trip (c3a 59.8 -> 56.0 us with L2
+    // flushed; the page-table prefetch in the decode instantiation measured
+    // 1 us slower on the batched decode).
     if (warp == 9) {
       const BlockDesc &b0 = head.blk;
       const int lane = tid & 31;
@@ -262,6 +263,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nline = (int)(reinterpret_cast<uintptr_t>(pt_row + e1) >> 7) - line0 + 1;
       if (lane < nline)
         asm volatile("prefetch.global.L2 [%0];\n" ::"l"(pt_row + min(e0 + lane * 32, e1)) : "memory");
+    } else if (warp >= 4 && warp < 8) {
+      const BlockDesc &b0 = head.blk;
+      const int ct = tid - 128;
+      for (int i = ct; i < b0.nrows * (kDqk / 64); i += 128) {
+        const int r = i / (kDqk / 64), part = i % (kDqk / 64);
+        const int flat = b0.row0 + r;
+        const uint16_t *row = static_cast<const uint16_t *>(a.q) +
+                              ((int64_t)(b0.tok0 + flat / a.group) * a.hq + b0.g * a.group + flat % a.group) * kDqk;
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row + part * 64) : "memory");
+      }
     }
   }
 
