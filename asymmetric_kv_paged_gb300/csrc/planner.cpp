@@ -179,8 +179,10 @@ attn_status_t build_host_plan(const attn_problem_t *p, int32_t num_sms, HostPlan
   constexpr int64_t kWholeBlockTiles = 8;
   // A CTA that goes on to a further segment pays for the switch (the finished
   // segment's epilogue, the next block's Q) with this many tiles of its share:
-  // measured, two-segment CTAs otherwise ended ~3-5 us after the others.
-  constexpr int64_t kSegSwitchTiles = 3;
+  // measured, two-segment CTAs otherwise ended ~3-5 us after the others
+  // (on the batched decode 4 tiles measured ~1.5% faster than 3, 5 and 6 no
+  // better than 4).
+  constexpr int64_t kSegSwitchTiles = 4;
   if (nb > 0) {
     const int64_t min_tiles = 2;
     int64_t remaining = total_tiles;
