@@ -318,15 +318,22 @@ int32_t replan_host(HostPlan *hp, const int32_t *seq_lens) {
   }
   const int64_t T = start[nb];
   const int64_t ctas = std::min<int64_t>(T, hp->num_ctas);
+  const int32_t charge = switch_charge(T, ctas);
+  const int64_t P = T + (int64_t)charge * nb;
+  const int32_t *st = start.data();
   hp->segs.clear();
   hp->seg_cta.clear();
   hp->cta_seg_begin.assign(hp->num_ctas + 1, 0);
   for (int32_t c = 0; c < hp->num_ctas; ++c) {
     if (c < ctas) {
-      const int64_t a = share_begin(c, T, ctas), e = share_begin(c + 1, T, ctas);
-      for (int32_t bi = block_at(start.data(), nb, a); bi < nb && start[bi] < e; ++bi) {
-        hp->segs.push_back(share_segment(bi, hp->blocks[bi], start[bi], start[bi + 1], a, e, c, T,
-                                         ctas, hp->key_tile));
+      const int64_t a = share_begin(c, P, ctas), e = share_begin(c + 1, P, ctas);
+      for (int32_t bi = block_at(st, nb, a, charge); bi < nb && block_pos(st, bi, charge) < e;
+           ++bi) {
+        const SegDesc sd = share_segment(bi, hp->blocks[bi], block_pos(st, bi, charge),
+                                         block_pos(st, bi + 1, charge), a, e, c, P, ctas,
+                                         hp->key_tile, charge);
+        if (sd.tile_end == sd.tile_begin) continue;   // the share ends in the block's charge
+        hp->segs.push_back(sd);
         hp->seg_cta.push_back(c);
       }
     }
@@ -336,7 +343,8 @@ int32_t replan_host(HostPlan *hp, const int32_t *seq_lens) {
   hp->multi_split_blocks = 0;
   for (int32_t bi = 0; bi < nb; ++bi) {
     BlockDesc &bd = hp->blocks[bi];
-    bd.num_splits = share_splits(start[bi], start[bi + 1], T, ctas);
+    bd.num_splits = share_splits(block_pos(st, bi, charge), block_pos(st, bi + 1, charge), P, ctas,
+                                 charge);
     bd.part_row_base = -1;
     if (bd.num_splits > 1) {
       bd.part_row_base = (int32_t)part;

@@ -85,13 +85,22 @@ __global__ void __launch_bounds__(kReplanThreads, 1) replan_kernel(const ReplanA
   cta_exclusive_scan(r.tile_start, r.nb);
   const int64_t T = r.tile_start[r.nb];
   const int64_t ctas = T < r.num_ctas ? T : r.num_ctas;
+  const int32_t charge = switch_charge(T, ctas);
+  const int64_t P = T + (int64_t)charge * r.nb;     // global positions
 
-  // segments per CTA, then their offsets
+  // segments per CTA (blocks its share holds tiles of), then their offsets
   for (int32_t c = tid; c < r.num_ctas; c += kReplanThreads) {
     int32_t cnt = 0;
     if (c < ctas) {
-      const int64_t a = share_begin(c, T, ctas), e = share_begin(c + 1, T, ctas);
-      cnt = block_at(r.tile_start, r.nb, e - 1) - block_at(r.tile_start, r.nb, a) + 1;
+      const int64_t a = share_begin(c, P, ctas), e = share_begin(c + 1, P, ctas);
+      for (int32_t bi = block_at(r.tile_start, r.nb, a, charge); bi < r.nb; ++bi) {
+        const int64_t gs = block_pos(r.tile_start, bi, charge);
+        if (gs >= e) break;
+        const SegDesc sd =
+            share_segment(bi, r.blocks[bi], gs, block_pos(r.tile_start, bi + 1, charge), a, e, c,
+                          P, ctas, r.key_tile, charge);
+        cnt += sd.tile_end > sd.tile_begin;
+      }
     }
     r.cta_seg_begin[c] = cnt;
   }
@@ -99,19 +108,22 @@ __global__ void __launch_bounds__(kReplanThreads, 1) replan_kernel(const ReplanA
   cta_exclusive_scan(r.cta_seg_begin, r.num_ctas);
 
   for (int32_t c = tid; c < ctas; c += kReplanThreads) {
-    const int64_t a = share_begin(c, T, ctas), e = share_begin(c + 1, T, ctas);
+    const int64_t a = share_begin(c, P, ctas), e = share_begin(c + 1, P, ctas);
     int32_t s = r.cta_seg_begin[c];
-    for (int32_t bi = block_at(r.tile_start, r.nb, a); bi < r.nb; ++bi) {
-      const int64_t gs = r.tile_start[bi];
+    for (int32_t bi = block_at(r.tile_start, r.nb, a, charge); bi < r.nb; ++bi) {
+      const int64_t gs = block_pos(r.tile_start, bi, charge);
       if (gs >= e) break;
-      r.segs[s++] = share_segment(bi, r.blocks[bi], gs, r.tile_start[bi + 1], a, e, c, T, ctas,
-                                   r.key_tile);
+      const SegDesc sd =
+          share_segment(bi, r.blocks[bi], gs, block_pos(r.tile_start, bi + 1, charge), a, e, c, P,
+                        ctas, r.key_tile, charge);
+      if (sd.tile_end > sd.tile_begin) r.segs[s++] = sd;
     }
   }
 
   // splits and partial-row offsets of every block
   for (int32_t bi = tid; bi < r.nb; bi += kReplanThreads) {
-    const int32_t ns = share_splits(r.tile_start[bi], r.tile_start[bi + 1], T, ctas);
+    const int32_t ns = share_splits(block_pos(r.tile_start, bi, charge),
+                                    block_pos(r.tile_start, bi + 1, charge), P, ctas, charge);
     r.blocks[bi].num_splits = ns;
     r.part_start[bi] = ns > 1 ? ns * r.blocks[bi].nrows : 0;
   }

@@ -10,8 +10,12 @@
 //   - its tiles take the global positions [start[bi], start[bi+1]) of the
 //     exclusive prefix sum `start` of the tile counts (T = start[nb] tiles);
 //   - with C' = min(C, T) working CTAs, CTA c takes positions
-//     [c*T/C', (c+1)*T/C') (equal shares, rounded down), so a block is cut
-//     wherever a share ends and each piece is one segment.
+//     [c*P/C', (c+1)*P/C') (equal shares, rounded down), so a block is cut
+//     wherever a share ends and each piece is one segment.  On shares of 32
+//     tiles or more every block is first given `charge` positions without a
+//     tile (P = T + charge * nb): the CTA whose share reaches into a block
+//     pays for its epilogue and Q staging with that much less work, as in the
+//     static deal.
 #pragma once
 #include <cstdint>
 
@@ -41,7 +45,20 @@ AKP_HD int32_t block_tile_count(int32_t klo, int32_t khi, int32_t tile) {
   return (khi - 1) / tile - klo / tile + 1;
 }
 
-// First global tile position of CTA c's share (c = ctas gives T).
+// Positions a CTA pays for reaching into a block (its epilogue, the next Q),
+// on shares of at least 8 such charges; 0 (plain tile shares) below.
+constexpr int32_t kReplanSwitchTiles = 4;
+AKP_HD int32_t switch_charge(int64_t T, int64_t ctas) {
+  return T >= 8 * kReplanSwitchTiles * ctas ? kReplanSwitchTiles : 0;
+}
+
+// First global position of block bi: its tiles' prefix plus a charge per
+// earlier block (the block's tiles start `charge` positions later).
+AKP_HD int64_t block_pos(const int32_t *start, int32_t bi, int32_t charge) {
+  return (int64_t)start[bi] + (int64_t)charge * bi;
+}
+
+// First global position of CTA c's share (c = ctas gives the total P).
 AKP_HD int64_t share_begin(int64_t c, int64_t T, int64_t ctas) { return c * T / ctas; }
 
 // CTA whose share holds global tile position x (0 <= x < T, ctas <= T): the
@@ -50,13 +67,13 @@ AKP_HD int32_t share_owner(int64_t x, int64_t T, int64_t ctas) {
   return (int32_t)(((x + 1) * ctas - 1) / T);
 }
 
-// Block holding global tile position x: the largest i in [0, nb) with
-// start[i] <= x (start strictly increasing, start[0] = 0, x < start[nb]).
-AKP_HD int32_t block_at(const int32_t *start, int32_t nb, int64_t x) {
+// Block holding global position x: the largest i in [0, nb) with
+// block_pos(i) <= x (positions strictly increasing, x < the total).
+AKP_HD int32_t block_at(const int32_t *start, int32_t nb, int64_t x, int32_t charge) {
   int32_t lo = 0, hi = nb - 1;
   while (lo < hi) {
     const int32_t mid = (lo + hi + 1) >> 1;
-    if (start[mid] <= x)
+    if (block_pos(start, mid, charge) <= x)
       lo = mid;
     else
       hi = mid - 1;
@@ -65,23 +82,26 @@ AKP_HD int32_t block_at(const int32_t *start, int32_t nb, int64_t x) {
 }
 
 // Segment of block bi inside CTA c's share [a, e), with the block at global
-// positions [gs, ge).
+// positions [gs, ge), its tiles at [gs + charge, ge); tile_begin == tile_end
+// when the share holds none of them (it ends in the block's charge).
 AKP_HD SegDesc share_segment(int32_t bi, const BlockDesc &bd, int64_t gs, int64_t ge, int64_t a,
-                             int64_t e, int32_t c, int64_t T, int64_t ctas, int32_t tile) {
+                             int64_t e, int32_t c, int64_t P, int64_t ctas, int32_t tile,
+                             int32_t charge) {
   const int32_t tb = bd.klo / tile;
-  const int64_t lo = a > gs ? a : gs;
+  const int64_t ts = gs + charge;
+  const int64_t lo = a > ts ? a : ts;
   const int64_t hi = e < ge ? e : ge;
   SegDesc s;
   s.block = bi;
-  s.tile_begin = tb + (int32_t)(lo - gs);
-  s.tile_end = tb + (int32_t)(hi - gs);
-  s.split = c - share_owner(gs, T, ctas);
+  s.tile_begin = tb + (int32_t)(lo - ts);
+  s.tile_end = hi > lo ? tb + (int32_t)(hi - ts) : s.tile_begin;
+  s.split = c - share_owner(ts, P, ctas);
   return s;
 }
 
-// Splits of block bi (global positions [gs, ge)).
-AKP_HD int32_t share_splits(int64_t gs, int64_t ge, int64_t T, int64_t ctas) {
-  return share_owner(ge - 1, T, ctas) - share_owner(gs, T, ctas) + 1;
+// Splits of block bi (global positions [gs, ge), tiles from gs + charge).
+AKP_HD int32_t share_splits(int64_t gs, int64_t ge, int64_t P, int64_t ctas, int32_t charge) {
+  return share_owner(ge - 1, P, ctas) - share_owner(gs + charge, P, ctas) + 1;
 }
 
 // The head record of a CTA whose segments are [s0, s1) (see CtaHead).

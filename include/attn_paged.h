@@ -126,7 +126,8 @@ attn_status_t attn_plan(const attn_problem_t *problem, int device, attn_plan_t *
  * Other fields as for attn_plan.  Each run first launches a one-CTA planner
  * kernel that reads the caller's device seq_lens and rewrites the plan's work
  * list in device memory (key ranges, equal shares of the key tiles for one CTA
- * per SM, splits, partial offsets); the attention kernel and the merge follow
+ * per SM, each block also counting 4 tiles on shares of 32 tiles or more,
+ * splits, partial offsets); the attention kernel and the merge follow
  * on the same stream.  The workspace reported covers every length vector
  * within the bounds.  Results equal those of a plan built for the run's
  * lengths, up to the floating-point order of the split merge.
