@@ -305,14 +305,18 @@ def test_run_argument_errors():
     torch.cuda.synchronize()
 
 
-def test_bad_page_id_sets_error_word():
+@pytest.mark.parametrize("n", [1, 40], ids=["decode", "prefill_staged"])
+def test_bad_page_id_sets_error_word(n):
     """A page id outside the pool is never dereferenced: its rows read as zero and
-    the plan's device error word records it."""
+    the plan's device error word records it (the split-KV kernel, and the
+    staging pass of a prefill plan)."""
     from asymmetric_kv_paged_gb300 import binding as B
-    w = W.make_workload(12, [200], [1], hq=8, hkv=1, page_size=16)
+    w = W.make_workload(12, [200], [n], hq=8, hkv=1, page_size=16)
     w.page_table = w.page_table.copy()
     w.page_table[0, 3] = w.num_pages + 5
     dw = _runner()(w)
+    if n > 1:
+        assert len(B.attn_plan_stage_units(dw.plan)) == 1
     dw.run()
     torch.cuda.synchronize()
     assert B.attn_get_device_error(dw.plan) & 1
