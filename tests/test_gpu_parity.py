@@ -442,7 +442,7 @@ def test_batch_without_query_rows():
     assert B.attn_get_device_error(dw.plan) == 0
 
 
-@pytest.mark.parametrize("seed", range(48))
+@pytest.mark.parametrize("seed", range(96))
 def test_parity_random_shapes(seed):
     """Seeded random problems, every output row against the oracle: ragged
     lengths and query counts (decode, verify, short and long prefill blocks, so
