@@ -29,6 +29,10 @@ CASES = [
 # 152 CTA shares each cover about 55 blocks
 _MANY = np.random.default_rng(77).integers(1, 41, 4200).tolist()
 CASES.append(("many_blocks", _MANY, [1] * len(_MANY), 4, 2, 16, 0, False, "bf16"))
+# ~10,000 key tiles over 152 CTAs: shares of 32 tiles or more, so the device
+# deal charges every block for the segment switch
+_LONG = np.random.default_rng(78).integers(8000, 20000, 24).tolist()
+CASES.append(("decode_charged_p128", _LONG, [1] * len(_LONG), 16, 2, 128, 0, True, "bf16"))
 SHRINK = [777, 300, 65, 1, 0]     # replay at bound - d (at least n)
 
 
@@ -93,6 +97,11 @@ def test_graph_replay_with_changing_lengths(case):
         assert np.array_equal(B.attn_plan_blocks(dw.plan), B.attn_plan_blocks(mirror))
         assert np.array_equal(B.attn_plan_segments(dw.plan), B.attn_plan_segments(mirror))
         assert np.array_equal(B.attn_plan_cta_heads(dw.plan), B.attn_plan_cta_heads(mirror))
+        if name == "decode_charged_p128":
+            # the switch charge is in force: CTAs that reach into more blocks hold fewer tiles
+            segs = B.attn_plan_segments(dw.plan)
+            loads = np.bincount(segs[:, 0], weights=segs[:, 3] - segs[:, 2])
+            assert loads.max() - loads.min() > 1
 
 
 def test_lengths_outside_bounds_are_clamped_and_flagged():
