@@ -24,7 +24,7 @@ EXPORTED = ("attn_plan", "attn_run_paged", "attn_run_phase", "attn_plan_destroy"
             "attn_status_string", "attn_plan_host", "attn_plan_info", "attn_plan_blocks",
             "attn_plan_segments", "attn_plan_cta_heads", "attn_plan_stage_units",
             "attn_plan_merge_ctas",
-            "attn_debug_tc_gemm",
+            "attn_debug_tc_gemm", "attn_debug_stamps",
             "attn_run_paged_no_workspace",
             "attn_append_kv", "attn_plan_replayable", "attn_plan_replayable_host",
             "attn_plan_replan_host", "attn_plan_fetch_device")
@@ -48,10 +48,21 @@ class AttnError(RuntimeError):
 
 
 _LIB = None
+_STAMPS = False      # load the profiling build (attn_debug_stamps records) instead
 
 
 def library_path() -> str:
-    return _build.lib_path()
+    return _build.lib_path(_STAMPS)
+
+
+def use_stamps_build() -> None:
+    """Make load() use the profiling build of the same sources, whose split-KV
+    kernel records timestamps (include/attn_paged_debug.h, attn_debug_stamps).
+    Call before the library is first loaded."""
+    global _STAMPS
+    if _LIB is not None and not _STAMPS:
+        raise RuntimeError("the default library is already loaded")
+    _STAMPS = True
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -59,7 +70,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     global _LIB
     if _LIB is not None:
         return _LIB
-    path = _build.build() if build_if_missing else library_path()
+    path = _build.build(stamps=_STAMPS) if build_if_missing else library_path()
     if not os.path.exists(path):
         raise RuntimeError(f"libattn_paged.so not found at {path}")
     L = ctypes.CDLL(path)
@@ -84,6 +95,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_plan_replan_host.argtypes = [vp, i32p, i32p]
     L.attn_plan_fetch_device.argtypes = [vp]
     L.attn_debug_tc_gemm.argtypes = [ctypes.c_int32] * 4 + [vp, vp, vp, vp, vp]
+    L.attn_debug_stamps.argtypes = [vp, ctypes.c_int32]
     for name in EXPORTED:
         if name != "attn_status_string":
             getattr(L, name).restype = ctypes.c_int
@@ -332,3 +344,18 @@ def attn_debug_tc_gemm(mode: int, variant: int, ab_type: int, n: int, a, b, d, s
     _check(load().attn_debug_tc_gemm(int(mode), int(variant), int(ab_type), int(n), _ptr(a),
                                      _ptr(b), _ptr(d), _ptr(status), ctypes.c_void_p(int(stream))),
            "attn_debug_tc_gemm")
+
+
+ATTN_DEBUG_STAMP_CTAS = 160
+ATTN_DEBUG_STAMP_EVENTS = 16
+
+
+def attn_debug_stamps(clear: bool = True):
+    """Timestamps of the split-KV kernel's last launches, a
+    [ATTN_DEBUG_STAMP_CTAS, ATTN_DEBUG_STAMP_EVENTS] uint64 array (profiling build
+    only; the default build raises ATTN_ERR_UNSUPPORTED)."""
+    import numpy as np
+    arr = np.zeros((ATTN_DEBUG_STAMP_CTAS, ATTN_DEBUG_STAMP_EVENTS), dtype=np.uint64)
+    _check(load().attn_debug_stamps(ctypes.c_void_p(arr.ctypes.data), int(bool(clear))),
+           "attn_debug_stamps")
+    return arr

@@ -40,11 +40,18 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "attn_paged_debug.h"
 #include "e4m3.cuh"
 #include "kernels.hpp"
+#include "stamps.cuh"
 #include "tc_common.cuh"
 
 namespace akp {
+
+#ifdef AKP_STAMPS
+__device__ unsigned long long g_stamps[kStampCtas * kStampEvents];
+#endif
+
 namespace {
 
 constexpr int kN = kKeyTile;                 // keys per tile (64)
@@ -240,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  if (tid == 0) AKP_STAMP(kStampStart);
   // Launched as a programmatic dependent (of the device planner or the KV
   // append, when they precede it): nothing they write is read before this wait.
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -254,6 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int seg_end = head.seg_end;
   if (seg_begin >= seg_end) return;
   const int total = head.total;
+  if (tid == 0) {
+    AKP_STAMP(kStampHead);
+    AKP_STAMP_VALUE(kStampSegs, seg_end - seg_begin);
+    AKP_STAMP_VALUE(kStampTiles, total);
+  }
   if constexpr (HALF) {
     // Verify plans: while the barriers are set up, the producer warp warms
     // the page-table entries of the CTA's first four tiles and the converter
@@ -325,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const uint32_t sbase = tc::smem_u32(smem);
+  if (tid == 0) AKP_STAMP(kStampReady);
   SlotBars *slot_bars = reinterpret_cast<SlotBars *>(smem + Lay::kOffSlotBars);
 
   if (warp == 9) {
@@ -374,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ring[r * kN + 2 * ln] = sl[u][0];
           ring[r * kN + 2 * ln + 1] = sl[u][1];
           tc::mbar_arrive(&slot_bars->full[r]);
+          if (k == 0 && ln == 0) AKP_STAMP(kStampFirstLoad);
         }
       }
     }
@@ -403,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               atomicOr(a.err, 1);
           }
         }
+        if (k == 0) AKP_STAMP(kStampLookup);
         uint64_t *empty = FP8 ? &bars.tma_empty[t] : &bars.op_empty[t];
         if (k >= NT && !tc::mbar_wait(empty, ((k / NT) - 1) & 1, &abort_flag)) break;
         // BF16: a tile with keys outside the block's range lands on edge_full, which
@@ -429,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           full);
           }
         }
+        if (k == 0) AKP_STAMP(kStampFirstLoad);
       }
     }
   } else if (warp >= 4 && warp < 8) {
@@ -481,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars.q_full[qb]);
+      if (ct == 0 && c.si == 0) AKP_STAMP(kStampFirstQ);
       return true;
     };
     if constexpr (FP8 && TMA) {
@@ -680,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_f16_ss(tmem + b * kN, ad, bdsc, id_s, kq > 0 ? 1u : 0u);
         }
         tc::mma_commit(&bars.s_full[b]);
+        if (ks == 0) AKP_STAMP(kStampFirstQK);
         if (FP8 && TMA) tc::mma_commit(&bars.k_empty[s]);
         if (cs.last()) tc::mma_commit(&bars.q_empty[qb]);
       }
@@ -715,6 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // overwritten now
         tc::mma_commit(&bars.op_empty[s]);
         tc::mma_commit(&bars.pv_done[b]);
+        if (kp == total - 1) AKP_STAMP(kStampLastPV);
       }
       tc::mma_commit(&bars.final_done);
       tc::mbar_wait(&bars.final_done, 0, &abort_flag);
@@ -979,6 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int b = k & 1;
       if (!wait(&bars.s_full[b], (k >> 1) & 1)) break;
+      if (t == 0 && k == 0) AKP_STAMP(kStampFirstS);
       tc::tc_fence_after();
       if (!tile_body(k)) break;
       tc::tc_fence_before();
@@ -987,6 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---------------- end of segment: normalise and write the block's rows
       if (!wait(&bars.pv_done[b], (k >> 1) & 1)) break;
+      if (t == 0) AKP_STAMP(kStampEpiBegin);
       if constexpr (HALF) {
         // the row's two halves: one denominator; the lower half writes the row
         // (its lane holds the row's O)
@@ -1137,12 +1159,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!sync_ok) break;
       }
+      if (t == 0) AKP_STAMP(kStampEpiEnd);
       tc::tc_fence_before();
       tc::mbar_arrive(&bars.o_free);
     }
   }
 
   __syncthreads();
+  if (tid == 0) AKP_STAMP(kStampEnd);
   if (tid == 0 && abort_flag) atomicOr(a.err, 2);
   if (warp == 8) {
     tc::tc_fence_after();
@@ -1215,3 +1239,27 @@ cudaError_t prepare_attn_tc(const HostPlan &hp) {
 }
 
 }  // namespace akp
+
+extern "C" attn_status_t attn_debug_stamps(uint64_t *host, int32_t clear) {
+#ifdef AKP_STAMPS
+  static_assert(akp::kStampCtas == ATTN_DEBUG_STAMP_CTAS &&
+                    akp::kStampEvents == ATTN_DEBUG_STAMP_EVENTS,
+                "stamp array shape");
+  if (!host) return ATTN_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(host, akp::g_stamps, sizeof(akp::g_stamps)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (clear) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, akp::g_stamps) != cudaSuccess ||
+        cudaMemset(p, 0, sizeof(akp::g_stamps)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+#else
+  (void)host;
+  (void)clear;
+  return ATTN_ERR_UNSUPPORTED;
+#endif
+}

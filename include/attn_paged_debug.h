@@ -55,6 +55,29 @@ attn_status_t attn_debug_tc_gemm(int32_t mode, int32_t variant, int32_t ab_type,
                                  const void *a, const void *b, float *d, int32_t *status,
                                  void *stream);
 
+/*
+ * Start-up and epilogue timestamps of the split-KV attention kernel, recorded
+ * only by a profiling build of the library (compiled with AKP_STAMPS; the
+ * default build returns ATTN_ERR_UNSUPPORTED and records nothing).  Each CTA
+ * with index below ATTN_DEBUG_STAMP_CTAS writes, on every launch, the GPU's
+ * global timer (ns) at fixed points of its run into row `cta` of a
+ * [ATTN_DEBUG_STAMP_CTAS][ATTN_DEBUG_STAMP_EVENTS] array of uint64:
+ *   0 first instruction, 1 head record read, 2 barriers and TMEM ready,
+ *   3 first tile's K/V requested, 4 first Q block staged, 5 first Q.K^T
+ *   issued, 6 first S tile ready, 7 last P.V issued, 8 / 9 begin / end of the
+ *   last segment's epilogue, 10 all roles done;
+ *   11 and 12 are counts, not times: the CTA's segments and key tiles;
+ *   13 first tile's page-table entries read (page sizes TMA can tile).
+ * Entries a launch does not reach keep their previous value (0 after a clear).
+ * attn_debug_stamps synchronises the current device, copies the array into
+ * `host` (ATTN_DEBUG_STAMP_CTAS * ATTN_DEBUG_STAMP_EVENTS values, caller-owned)
+ * and, if `clear` is nonzero, zeroes it on the device.
+ * Errors: UNSUPPORTED (default build), INVALID_ARG (host NULL), CUDA.
+ */
+#define ATTN_DEBUG_STAMP_CTAS 160
+#define ATTN_DEBUG_STAMP_EVENTS 16
+attn_status_t attn_debug_stamps(uint64_t *host, int32_t clear);
+
 #ifdef __cplusplus
 }
 #endif

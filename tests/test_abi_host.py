@@ -31,6 +31,13 @@ def test_library_exports_every_declared_symbol():
     assert set(declared) == set(B.EXPORTED)
 
 
+def test_stamps_are_only_in_the_profiling_build():
+    # the default build records no timestamps: the entry point exists and says so
+    with pytest.raises(B.AttnError) as e:
+        B.attn_debug_stamps(clear=False)
+    assert e.value.status == B.ATTN_ERR_UNSUPPORTED
+
+
 def test_status_strings():
     assert B.attn_status_string(0) == "ok"
     assert "workspace" in B.attn_status_string(B.ATTN_ERR_WORKSPACE)
