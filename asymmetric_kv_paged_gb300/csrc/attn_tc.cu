@@ -266,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     AKP_STAMP(kStampHead);
     AKP_STAMP_VALUE(kStampSegs, seg_end - seg_begin);
     AKP_STAMP_VALUE(kStampTiles, total);
+    AKP_STAMP_SMID(kStampSm);
   }
   if constexpr (HALF) {
     // Verify plans: while the barriers are set up, the producer warp warms

@@ -29,6 +29,7 @@ enum StampEvent : int {
   kStampSegs = 11,      // value: segments of the CTA
   kStampTiles = 12,     // value: key tiles of the CTA
   kStampLookup = 13,    // producer: first tile's page-table entries read (TMA paths)
+  kStampSm = 14,        // value: the SM the CTA runs on (%smid)
 };
 
 }  // namespace akp
@@ -48,7 +49,16 @@ enum StampEvent : int {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                       \
     AKP_STAMP_VALUE(ev, t_);                                                      \
   } while (0)
+#define AKP_STAMP_SMID(ev)                                                        \
+  do {                                                                            \
+    unsigned sm_;                                                                 \
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                             \
+    AKP_STAMP_VALUE(ev, sm_);                                                     \
+  } while (0)
 #else
+#define AKP_STAMP_SMID(ev) \
+  do {                     \
+  } while (0)
 #define AKP_STAMP_VALUE(ev, v) \
   do {                         \
   } while (0)

@@ -5,6 +5,13 @@ attn_debug_stamps).
 
     python -m asymmetric_kv_paged_gb300.startup_trace c1_tiny_decode c4_swa_sinks
 
+Per-SM stream rate: for CTAs with one segment, the time from the first S tile to
+the last P.V divided by their key tiles (``tile_us``: minimum, median, maximum
+over CTAs of its mean over the runs), whether each CTA ran on the same SM in
+every run (``same_sm``: fraction of CTAs), and the correlation of each CTA's
+rate between the first and second half of the runs (``rate_repeat``; near 1
+when some SMs are persistently slower than others).
+
 For each named workload the attention kernel alone (no merge) is launched
 ``--runs`` times after three warm-up steps, each time after L2 has been flushed
 (a 256 MB buffer written and read back, as bench.py does between steps) and,
@@ -27,7 +34,7 @@ import numpy as np
 EVENTS = (("start", 0), ("head", 1), ("ready", 2), ("lookup", 13), ("first_load", 3),
           ("first_q", 4), ("first_qk", 5), ("first_s", 6), ("last_pv", 7), ("epi_begin", 8),
           ("epi_end", 9), ("end", 10))
-SEGS, TILES = 11, 12
+SEGS, TILES, SM = 11, 12, 14
 
 
 def _stats(stamps: np.ndarray, ctas: int) -> dict:
@@ -70,7 +77,7 @@ def trace(name: str, runs: int, flush: bool) -> dict:
     torch.cuda.synchronize()
     B.attn_debug_stamps(clear=True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    per_run, times = [], []
+    per_run, times, raw = [], [], []
     for _ in range(runs):
         if flush:
             buf.fill_(1)
@@ -84,7 +91,9 @@ def trace(name: str, runs: int, flush: bool) -> dict:
         e1.record(st)
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1) * 1e3)
-        per_run.append(_stats(B.attn_debug_stamps(clear=True), ctas))
+        stamps = B.attn_debug_stamps(clear=True)
+        per_run.append(_stats(stamps, ctas))
+        raw.append(stamps[:min(ctas, stamps.shape[0])].astype(np.int64))
         dw.run_phase(1, st)
     torch.cuda.synchronize()
     assert B.attn_get_device_error(dw.plan) == 0
@@ -95,7 +104,26 @@ def trace(name: str, runs: int, flush: bool) -> dict:
         vals = [r[key] for r in per_run if key in r]
         if vals:
             out[key] = [round(float(np.median([v[j] for v in vals])), 2) for j in range(3)]
+    out.update(_sm_rates(np.stack(raw)))
     return out
+
+
+def _sm_rates(raw: np.ndarray) -> dict:
+    """Stream rate of the one-segment CTAs and how it repeats across runs
+    (raw: runs x CTAs x events)."""
+    one = (raw[0, :, SEGS] == 1) & (raw[0, :, TILES] > 0) & np.all(raw[:, :, 0] > 0, axis=0)
+    if one.sum() < 2 or raw.shape[0] < 2:
+        return {}
+    x = raw[:, one]
+    rate = (x[:, :, 7] - x[:, :, 6]) / 1e3 / x[:, :, TILES]     # runs x CTAs, us per tile
+    mean = rate.mean(axis=0)
+    h = rate.shape[0] // 2
+    rep = np.corrcoef(rate[:h].mean(axis=0), rate[h:].mean(axis=0))[0, 1]
+    same = float(np.mean([np.unique(x[:, c, SM]).size == 1 for c in range(x.shape[1])]))
+    return {"tile_us": [round(float(mean.min()), 3), round(float(np.median(mean)), 3),
+                        round(float(mean.max()), 3)],
+            "one_segment_ctas": int(one.sum()), "same_sm": round(same, 2),
+            "rate_repeat": round(float(rep), 2)}
 
 
 def main() -> None:

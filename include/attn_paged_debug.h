@@ -67,7 +67,8 @@ attn_status_t attn_debug_tc_gemm(int32_t mode, int32_t variant, int32_t ab_type,
  *   issued, 6 first S tile ready, 7 last P.V issued, 8 / 9 begin / end of the
  *   last segment's epilogue, 10 all roles done;
  *   11 and 12 are counts, not times: the CTA's segments and key tiles;
- *   13 first tile's page-table entries read (page sizes TMA can tile).
+ *   13 first tile's page-table entries read (page sizes TMA can tile);
+ *   14 a value: the index of the SM the CTA ran on.
  * Entries a launch does not reach keep their previous value (0 after a clear).
  * attn_debug_stamps synchronises the current device, copies the array into
  * `host` (ATTN_DEBUG_STAMP_CTAS * ATTN_DEBUG_STAMP_EVENTS values, caller-owned)
